@@ -1,0 +1,425 @@
+"""Benchmark of the GDN ReplaySSM hot path: verify -> accept -> flush over a
+24-layer decode sweep (B=32 sequences, H=16 heads, d_k=d_v=128, T=16 draft
+tokens, flush threshold 32, accepted counts ~ geometric with mean 12 capped at
+16), on one GPU per rank.
+
+One step = for each of the 24 layers: gdn_replay_verify, gdn_replay_accept,
+gdn_replay_flush (the flush enqueues its length epilogue as a second kernel).
+Every layer keeps its own checkpoint and buffer, so one step streams
+24 x 33.5 MB of state -- far larger than L2; no extra L2 flush is needed.
+
+Prints one JSON line (rank 0).  value = microseconds per layer-step, i.e. the
+device time of K steps divided by 24*K (and by the number of ranks, whose
+replicas run side by side with no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+WORKLOAD = "decode24"
+DRAFT_POOL = 4          # distinct draft blocks per layer, cycled over steps
+ACCEPT_PERIOD = 16      # distinct accepted-count patterns, cycled over steps
+FALLBACK_HBM_GBS = 6800.0
+# dram read+write bytes per verify launch from the ncu capture summarised in
+# profiles/; valid only for the kernel source whose hash is recorded with it.
+NCU_TRAFFIC = {}        # {source_sha1: bytes_per_launch}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------ host bookkeeping
+def bytes_model(wl, lens_before, acc):
+    """Algorithmic HBM bytes of one layer-step given the lengths before verify
+    and the accepted counts.  Returns (verify, accept, flush, new_lens, n_flushed_tokens)."""
+    eb = 2 if wl.in_dtype == "bf16" else 4
+    H, dk, dv, T = wl.H, wl.dk, wl.dv, wl.T
+    st = dv * dk * 4
+    tok_buf = (dk + dv) * eb + 8                         # one buffered token (k, v, g, beta)
+    L = lens_before.astype(np.int64)
+    verify = H * (st * len(L) + tok_buf * L.sum()
+                  + len(L) * T * ((2 * dk + dv) * eb + 8)   # draft q, k, v, g, beta read
+                  + len(L) * T * tok_buf                    # draft staged into the buffer
+                  + len(L) * T * dv * 4)                    # outputs
+    accept = len(L) * 12
+    new = L + acc.astype(np.int64)
+    fl = new >= wl.threshold
+    flush = H * (2 * st * fl.sum() + tok_buf * new[fl].sum()) + len(L) * 8
+    new2 = np.where(fl, 0, new)
+    return verify, accept, flush, new2, int(new[fl].sum())
+
+
+def clocks_sampler():
+    q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    dev = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0] or str(torch.cuda.current_device())
+    try:
+        return subprocess.Popen(["nvidia-smi", "-i", dev, f"--query-gpu={q}", "--format=csv,noheader",
+                                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                text=True)
+    except (FileNotFoundError, ValueError):
+        return None
+
+
+def clocks_summary(proc):
+    if proc is None:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+    proc.terminate()
+    try:
+        out, _ = proc.communicate(timeout=5)
+    except subprocess.TimeoutExpired:
+        proc.kill()
+        out, _ = proc.communicate()
+    sm, smax, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in out.strip().splitlines():
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 9:
+            continue
+        try:
+            sm.append(float(f[1].split()[0]))
+            smax.append(float(f[2].split()[0]))
+        except ValueError:
+            continue
+        for n, v in zip(names, f[5:9]):
+            if v.lower() == "active":
+                reasons.add(n)
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for key in ("hbm_gbs", "hbm_GBps", "hbm"):
+                if key in d and isinstance(d[key], (int, float)):
+                    return float(d[key]), "measured"
+        except (ValueError, OSError):
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_sha1():
+    h = hashlib.sha1()
+    for rel in ("speculative_decode_recurrent_gb300/csrc/gdn_replay.cu",):
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
+    return h.hexdigest()
+
+
+# ----------------------------------------------------------------- CPU oracle
+def cpu_oracle_run(wl, seconds, steps_cap=None):
+    """Time the CPU oracle on layer 0 of the workload until `seconds` elapse.
+    Returns (seconds, layer_steps, threads, b_sample)."""
+    import oracle
+    threads = os.cpu_count() or 1
+    B = wl.B
+    init = synth.initial_layer(wl, 0)
+    d = oracle.Dims(B=B, H=wl.H, dk=wl.dk, dv=wl.dv, T=wl.T, cap=wl.cap, threshold=wl.threshold,
+                    n_slot=init["state"].shape[0], scale=wl.scale, n_threads=threads)
+    layer = oracle.Layer(d, init)
+    blocks = [synth.draft_block(wl, 0, s) for s in range(DRAFT_POOL)]
+    n, t0 = 0, time.perf_counter()
+    while True:
+        blk = blocks[n % DRAFT_POOL]
+        layer.verify(blk)
+        layer.accept(_accept_pattern(wl, 0, n % ACCEPT_PERIOD))
+        layer.flush()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or (steps_cap and n >= steps_cap):
+            return el, n, threads, B
+
+
+def _accept_pattern(wl, layer, j):
+    return synth.workloads.accepted_counts(wl, layer, 1000 + j).numpy()
+
+
+# ------------------------------------------------------------------- GPU run
+def run_ours(args, rank, world):
+    import speculative_decode_recurrent_gb300 as lib
+
+    wl = synth.WORKLOADS[WORKLOAD]
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    lib.load()
+    from speculative_decode_recurrent_gb300 import Dims, ReplayLayer
+    n_slot = wl.n_slot
+    d = Dims(B=wl.B, H=wl.H, dk=wl.dk, dv=wl.dv, T=wl.T, cap=wl.cap, threshold=wl.threshold,
+             n_slot=n_slot, in_dtype=lib.DTYPE_BF16, scale=wl.scale)
+    L = wl.layers
+    layers, pools, acc_dev, acc_host = [], [], [], []
+    lens0 = []
+    for l in range(L):
+        init = synth.initial_layer(wl, l + 100 * rank)
+        layers.append(ReplayLayer(d, init, dev))
+        lens0.append(init["buf_len"][init["state_idx"].long()].numpy().astype(np.int64))
+        pools.append([{n: t.to(dev) for n, t in synth.draft_block(wl, l + 100 * rank, s).items()}
+                      for s in range(DRAFT_POOL)])
+        pats = np.stack([_accept_pattern(wl, l + 100 * rank, j) for j in range(ACCEPT_PERIOD)])
+        acc_host.append(pats)
+        acc_dev.append(torch.from_numpy(pats).to(dev))
+    outs = [torch.empty(wl.B, wl.T, wl.H, wl.dv, device=dev) for _ in range(L)]
+    stream = torch.cuda.Stream(device=dev)
+
+    def enqueue_step(j, events=None):
+        for l in range(L):
+            blk = pools[l][j % DRAFT_POOL]
+            if events is not None:
+                events[l][0].record()
+            layers[l].verify(blk["q"], blk["k"], blk["v"], blk["g"], blk["beta"], outs[l])
+            if events is not None:
+                events[l][1].record()
+            layers[l].accept(acc_dev[l][j])
+            if events is not None:
+                events[l][2].record()
+            layers[l].flush(force=False)
+            if events is not None:
+                events[l][3].record()
+
+    # one graph per accepted-count pattern (and draft-pool entry)
+    graphs = []
+    with torch.cuda.stream(stream):
+        torch.cuda.synchronize()
+        for j in range(ACCEPT_PERIOD):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                enqueue_step(j)
+            graphs.append(g)
+    # capture leaves the layers untouched (nothing ran); simulate lengths on the host
+    lens = [x.copy() for x in lens0]
+    tot = {"verify": 0, "accept": 0, "flush": 0, "tokens": 0}
+
+    def account(j):
+        for l in range(L):
+            v, a, f, new, _ = bytes_model(wl, lens[l], acc_host[l][j])
+            tot["verify"] += v; tot["accept"] += a; tot["flush"] += f
+            tot["tokens"] += int(acc_host[l][j].sum())
+            lens[l] = new
+
+    for s in range(args.warmup):
+        graphs[s % ACCEPT_PERIOD].replay()
+        account(s % ACCEPT_PERIOD)
+    torch.cuda.synchronize()
+    for k in tot:
+        tot[k] = 0
+    if world > 1:
+        torch.distributed.barrier()
+    sampler = clocks_sampler() if rank == 0 else None
+    time.sleep(0.1 if sampler else 0)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record()
+        for s in range(args.warmup, args.warmup + args.steps):
+            graphs[s % ACCEPT_PERIOD].replay()
+        e1.record()
+    for s in range(args.warmup, args.warmup + args.steps):
+        account(s % ACCEPT_PERIOD)
+    torch.cuda.synchronize()
+    clocks = clocks_summary(sampler) if rank == 0 else None
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    # the device lengths must follow the host bookkeeping exactly
+    for l in range(L):
+        got = layers[l].t["buf_len"][layers[l].t["state_idx"].long()].cpu().numpy()
+        if not np.array_equal(got, lens[l]) or int(layers[l].status.item()) != 0:
+            raise RuntimeError(f"layer {l}: device lengths/status diverge from the bookkeeping")
+    timed_bytes = dict(tot)
+
+    # ---- per-kernel durations: the same steps with timing events between kernels
+    try:
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+               for _ in range(L)]
+        per_k = {"verify": [], "accept": [], "flush": []}
+        kb = {"verify": 0, "flush": 0}
+        n_inst = min(args.steps, 2 * ACCEPT_PERIOD)
+        igraphs = []
+        with torch.cuda.stream(stream):
+            for j in range(ACCEPT_PERIOD):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    enqueue_step(j, evs)
+                igraphs.append(g)
+        start = args.warmup + args.steps
+        for s in range(start, start + n_inst):
+            j = s % ACCEPT_PERIOD
+            with torch.cuda.stream(stream):
+                igraphs[j].replay()
+            stream.synchronize()
+            for l in range(L):
+                per_k["verify"].append(evs[l][0].elapsed_time(evs[l][1]))
+                per_k["accept"].append(evs[l][1].elapsed_time(evs[l][2]))
+                per_k["flush"].append(evs[l][2].elapsed_time(evs[l][3]))
+                v, a, f, new, _ = bytes_model(wl, lens[l], acc_host[l][j])
+                kb["verify"] += v; kb["flush"] += f
+                lens[l] = new
+        kern_ms = {k: float(np.mean(v)) for k, v in per_k.items()}
+        verify_bytes_per_launch = kb["verify"] / (n_inst * L)
+        flush_bytes_per_launch = kb["flush"] / (n_inst * L)
+    except TypeError:
+        kern_ms, verify_bytes_per_launch, flush_bytes_per_launch = None, None, None
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        pin = [{n: t.cpu().pin_memory() for n, t in synth.draft_block(wl, l + 100 * rank, 0).items()}
+               for l in range(L)]
+        out_host = [torch.empty_like(outs[l], device="cpu").pin_memory() for l in range(L)]
+        stage = [pools[l][0] for l in range(L)]
+        acc_stage = [torch.empty(wl.B, dtype=torch.int32, device=dev) for _ in range(L)]
+        acc_pin = [torch.from_numpy(acc_host[l][0].copy()).pin_memory() for l in range(L)]
+        ge = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(ge, stream=stream):
+                for l in range(L):
+                    b = stage[l]
+                    layers[l].verify(b["q"], b["k"], b["v"], b["g"], b["beta"], outs[l])
+                    layers[l].accept(acc_stage[l])
+                    layers[l].flush(force=False)
+        h2d = sum(sum(t.numel() * t.element_size() for n, t in pin[l].items() if n != "accepted")
+                  + acc_pin[l].numel() * 4 for l in range(L))
+        d2h = sum(o.numel() * o.element_size() for o in outs)
+        torch.cuda.synchronize()
+        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            x0.record()
+            for s in range(args.e2e_steps):
+                for l in range(L):
+                    for n in ("q", "k", "v", "g", "beta"):
+                        stage[l][n].copy_(pin[l][n], non_blocking=True)
+                    acc_stage[l].copy_(acc_pin[l], non_blocking=True)
+                ge.replay()
+                for l in range(L):
+                    out_host[l].copy_(outs[l], non_blocking=True)
+            x1.record()
+        torch.cuda.synchronize()
+        e2e_ms = x0.elapsed_time(x1)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": round(e2e_ms * 1000.0 / (args.e2e_steps * L * world), 3), "unit": "us/layer",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "steps": args.e2e_steps}
+
+    return dict(ms=ms, clocks=clocks, timed_bytes=timed_bytes, kern_ms=kern_ms,
+                verify_bpl=verify_bytes_per_launch, flush_bpl=flush_bytes_per_launch, e2e=e2e, L=L)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    wl = synth.WORKLOADS[WORKLOAD]
+    workload_desc = (f"{WORKLOAD}: {wl.layers} GDN layers x B={wl.B}, H={wl.H}, dk=dv={wl.dk}, "
+                     f"T={wl.T}, flush threshold {wl.threshold}, accepts min(16, geometric mean 12)")
+    metric = "GDN verify+accept+flush time per layer-step at B=32,H=16,d=128,T=16"
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        # the CPU oracle, as it stands, on this arm's workload: each step is one
+        # layer-step of layer 0 at full batch, on all host cores
+        import oracle
+        oracle.build()
+        budget = 120.0
+        per = max(1, args.warmup + args.steps)
+        t0 = time.perf_counter()
+        el, n, threads, B = cpu_oracle_run(wl, seconds=min(budget, 1e9), steps_cap=per)
+        us = el * 1e6 / n
+        steps_timed = n
+        line = {"impl": "reference", "metric": metric, "value": round(us, 3), "unit": "us/layer",
+                "n_gpus": args.gpus, "steps": steps_timed, "warmup": 0,
+                "ms_per_step": round(us / 1000.0, 4), "higher_is_better": False, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": workload_desc, "l2": "n/a (CPU)"},
+                "cpu_baseline": {"value": round(us, 3), "unit": "us/layer", "cores": threads,
+                                 "kind": "oracle",
+                                 "sample": f"layer 0, B={B}, {n} consecutive layer-steps "
+                                           f"(capped at steps+warmup and {budget:.0f} s)"},
+                "e2e": {"value": round(us, 3), "unit": "us/layer", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0},
+                "wall_s": round(time.perf_counter() - t0, 2)}
+        print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device(
+            "cuda", int(os.environ.get("LOCAL_RANK", 0))))
+    r = run_ours(args, rank, world)
+    if rank == 0:
+        L = r["L"]
+        us_layer = r["ms"] * 1000.0 / (args.steps * L * world)
+        tb = r["timed_bytes"]
+        total_bytes = tb["verify"] + tb["accept"] + tb["flush"]
+        gbs = total_bytes / (r["ms"] * 1e-3) / 1e9 * world
+        peak, peak_kind = hbm_peak()
+        roof = None
+        if r["kern_ms"]:
+            ach = r["verify_bpl"] / (r["kern_ms"]["verify"] * 1e-3) / 1e9
+            traffic = NCU_TRAFFIC.get(source_sha1())
+            roof = {"bound": "hbm", "kernel": "verify", "achieved": round(ach, 1),
+                    "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
+                    "peak_source": f"{peak_kind} HBM copy bandwidth",
+                    "traffic": traffic,
+                    "algorithmic_bytes_per_launch": int(r["verify_bpl"]),
+                    "kernel_us": {k: round(v * 1000.0, 3) for k, v in r["kern_ms"].items()},
+                    "flush_achieved_gbs": round(r["flush_bpl"] / (r["kern_ms"]["flush"] * 1e-3) / 1e9, 1)}
+        cpu = None
+        if not args.no_cpu_baseline:
+            el, n, threads, B = cpu_oracle_run(synth.WORKLOADS[WORKLOAD], args.cpu_seconds)
+            cpu = {"value": round(el * 1e6 / n, 3), "unit": "us/layer", "cores": threads,
+                   "kind": "oracle", "sample": f"layer 0, B={B}, {n} consecutive layer-steps "
+                                               f"(~{args.cpu_seconds:.0f} s of fp64 C on host cores)"}
+        line = {"metric": metric, "value": round(us_layer, 3), "unit": "us/layer", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(r["ms"] / args.steps, 4), "higher_is_better": False,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": {"workload": workload_desc,
+                           "l2": "inputs larger than L2 (24 layers x 33.5 MB state rotate per step)",
+                           "parallelism": f"replicas x{world} (batch-sharded, no collective)",
+                           "draft_pool": DRAFT_POOL, "accept_period": ACCEPT_PERIOD},
+                "tokens_per_s": round(tb["tokens"] / L / (r["ms"] * 1e-3) * world, 1),
+                "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4),
+                "algorithmic_bytes_per_step": int(total_bytes / args.steps),
+                "roofline": roof, "cpu_baseline": cpu, "e2e": r["e2e"],
+                "gpu_launches": 4 * L * args.steps, "clocks": r["clocks"]}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

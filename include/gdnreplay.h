@@ -1,0 +1,147 @@
+/*
+ * gdnreplay.h -- C ABI of libgdnreplay: ReplaySSM-style verify / accept / flush
+ * of Gated DeltaNet (GDN) recurrent state under speculative decoding, as
+ * hand-written CUDA kernels for sm_103a (GB300).
+ *
+ * Method ("The inference stack behind OCRia", LlamaIndex engineering blog,
+ * section "Making speculative verification cheaper"): a GDN layer summarises
+ * history in a fixed-size recurrent state that each token reads from HBM,
+ * updates and writes back.  ReplaySSM instead keeps a checkpoint of the state
+ * plus a small buffer of recent inputs, computes outputs from the checkpoint
+ * and the buffered inputs, updates the full checkpoint only at a periodic
+ * flush, and on rejection moves the buffer pointer so that only the accepted
+ * prefix stays (no full-state restore).  The acceptance rule keeps the draft
+ * tokens before the first rejected one ("Inference Engineering", chapter 5,
+ * speculative decoding).
+ *
+ * Recurrence (the gated delta rule of "Gated Delta Networks", Yang, Kautz &
+ * Hatamizadeh, ICLR 2025; the blog names GDN without printing it), per
+ * sequence b and head h, with state S of shape [d_v, d_k]:
+ *     S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *     o_t = S_t (scale q_t),   alpha_t = exp(g_t),   scale = 1/sqrt(d_k)
+ * q and k arrive L2-normalised; the kernels do not re-normalise them.
+ *
+ * Layouts (row-major, innermost last; every tensor dense and contiguous):
+ *   state      fp32     [n_slot, H, dv, dk]   checkpoint per state slot
+ *   state_idx  int32    [B]                   slot of batch row b; NULL = identity
+ *                                             (slots must be distinct, < n_slot)
+ *   buf_k      in_dtype [n_slot, H, cap, dk]  committed (and staged draft) keys
+ *   buf_v      in_dtype [n_slot, H, cap, dv]
+ *   buf_g      fp32     [n_slot, H, cap]      log-decay g (alpha = exp(g)), g <= 0
+ *   buf_beta   fp32     [n_slot, H, cap]
+ *   buf_len    int32    [n_slot]              committed tokens in the buffer
+ *   q, k       in_dtype [B, T, H, dk]         draft block
+ *   v          in_dtype [B, T, H, dv]
+ *   g, beta    fp32     [B, T, H]
+ *   out        fp32     [B, T, H, dv]
+ *   accepted   int32    [B]                   accepted draft tokens, 0..T
+ *   status     int32    [1]                   device word; kernels OR fault bits in
+ * in_dtype is bf16 (GDN_DTYPE_BF16) or fp32 (GDN_DTYPE_F32).
+ * All pointers except dims are DEVICE pointers; dims is a host pointer read
+ * during the call only.
+ *
+ * Ownership and concurrency: the caller owns every buffer.  The library never
+ * allocates, frees or synchronises, and keeps no global state; each call only
+ * enqueues kernels on the given stream and returns.  Calls on one layer's
+ * buffers must be stream-ordered.
+ *
+ * Errors: 0 on success.  Host-side validation returns a negative code before
+ * anything is launched (see GDN_ERR_*).  Faults found on the device (a bad
+ * accepted count, no room in the buffer, a corrupt length) never trap: the
+ * kernel ORs a GDN_STATUS_* bit into *status, skips the affected sequence and
+ * continues.  Read *status after the stream has completed.
+ */
+#ifndef GDNREPLAY_H
+#define GDNREPLAY_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *cudaStream_t;
+
+#define GDN_DTYPE_BF16 0
+#define GDN_DTYPE_F32  1
+
+#define GDN_OK            0
+#define GDN_ERR_NULL     -1   /* a required pointer is NULL */
+#define GDN_ERR_DIMS     -2   /* unsupported or inconsistent dims */
+#define GDN_ERR_DTYPE    -3   /* in_dtype is not GDN_DTYPE_BF16 / GDN_DTYPE_F32 */
+#define GDN_ERR_LAUNCH   -4   /* the CUDA launch itself failed (cudaGetLastError) */
+
+#define GDN_STATUS_BAD_ACCEPT 1   /* accepted[b] outside [0, T]; b left unchanged */
+#define GDN_STATUS_NO_ROOM    2   /* verify: buf_len + T > cap; b skipped */
+#define GDN_STATUS_BAD_LEN    4   /* buf_len outside [0, cap] (accept: len + p > cap); b skipped */
+#define GDN_STATUS_BAD_SLOT   8   /* state_idx[b] outside [0, n_slot); b skipped */
+
+typedef struct {
+    int32_t B;          /* batch rows (sequences) in this call, >= 0 */
+    int32_t H;          /* heads, >= 1 */
+    int32_t dk;         /* key/query head dim: 64 or 128 */
+    int32_t dv;         /* value head dim (state rows): 64 or 128 */
+    int32_t T;          /* draft block length, 1..64 */
+    int32_t cap;        /* buffer slots per (slot, head), T <= cap <= 256 */
+    int32_t threshold;  /* flush when buf_len >= threshold, 1..cap */
+    int32_t n_slot;     /* state / buffer slots, >= B */
+    int32_t in_dtype;   /* GDN_DTYPE_BF16 or GDN_DTYPE_F32 */
+    float   scale;      /* query scale, normally 1/sqrt(dk) */
+} gdn_replay_dims;
+
+/*
+ * gdn_replay_verify -- "computes outputs from the checkpoint and the buffered
+ * inputs" (blog, "Making speculative verification cheaper").
+ * For every b with slot s = state_idx[b] and len = buf_len[s], and every head:
+ * start from state[s,h], replay the len committed tokens of the buffer, then
+ * the T draft tokens, writing o_t = S_t (scale q_t) to out[b,t,h,:] for each
+ * draft token.  The checkpoint and buf_len are NOT written.  The draft
+ * (k, v, g, beta) is copied into buffer slots [len, len+T) so that accepting p
+ * tokens later is a pure length update.  If len < 0 or len + T > cap the
+ * sequence is skipped (out untouched) and GDN_STATUS_NO_ROOM is set.
+ */
+int gdn_replay_verify(const gdn_replay_dims *dims,
+                      const float *state, const int32_t *state_idx,
+                      void *buf_k, void *buf_v, float *buf_g, float *buf_beta,
+                      const int32_t *buf_len,
+                      const void *q, const void *k, const void *v,
+                      const float *g, const float *beta,
+                      float *out, int32_t *status, cudaStream_t stream);
+
+/*
+ * gdn_replay_accept -- rollback/commit "adjusts the buffer pointer to keep the
+ * accepted prefix" (blog, same section): buf_len[s] += accepted[b] when
+ * 0 <= accepted[b] <= T and the result fits in cap; rejected draft tokens stay
+ * in the buffer as stale slots that the next verify overwrites.  Otherwise a
+ * status bit is set and buf_len[s] is left unchanged.  Writes only buf_len.
+ */
+int gdn_replay_accept(const gdn_replay_dims *dims, int32_t *buf_len,
+                      const int32_t *state_idx, const int32_t *accepted,
+                      int32_t *status, cudaStream_t stream);
+
+/*
+ * gdn_replay_flush -- "updates the full checkpoint only at periodic flush"
+ * (blog, same section).  For every b whose len = buf_len[s] satisfies
+ * len >= threshold, or len > 0 when force != 0: replay the len buffered tokens
+ * onto state[s,h] for every head, write the result back in place (fp32) and set
+ * buf_len[s] = 0.  Other sequences are left bit-identical.  A len outside
+ * [0, cap] sets GDN_STATUS_BAD_LEN and skips the sequence.
+ */
+int gdn_replay_flush(const gdn_replay_dims *dims, float *state,
+                     const int32_t *state_idx,
+                     const void *buf_k, const void *buf_v,
+                     const float *buf_g, const float *buf_beta,
+                     int32_t *buf_len, int32_t force, int32_t *status,
+                     cudaStream_t stream);
+
+/* Human-readable text for a GDN_ERR_* code (static storage). */
+const char *gdn_replay_strerror(int code);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int gdn_replay_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDNREPLAY_H */

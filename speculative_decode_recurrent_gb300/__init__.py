@@ -1,0 +1,159 @@
+"""Python binding of libgdnreplay (ReplaySSM verify / accept / flush of Gated
+DeltaNet state on sm_103a).
+
+Argument marshalling only: every step of the path runs in the CUDA kernels of
+``csrc/gdn_replay.cu`` behind the C ABI declared in ``include/gdnreplay.h``.
+PyTorch supplies device memory and the current stream.  There is no CPU
+fallback: if the shared library cannot be built or loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = ["Dims", "GdnError", "load", "gdn_replay_verify", "gdn_replay_accept",
+           "gdn_replay_flush", "gdn_replay_strerror", "STATUS_BAD_ACCEPT", "STATUS_NO_ROOM",
+           "STATUS_BAD_LEN", "DTYPE_BF16", "DTYPE_F32", "ReplayLayer"]
+
+DTYPE_BF16, DTYPE_F32 = 0, 1
+STATUS_BAD_ACCEPT, STATUS_NO_ROOM, STATUS_BAD_LEN, STATUS_BAD_SLOT = 1, 2, 4, 8
+_TORCH_IN = {DTYPE_BF16: torch.bfloat16, DTYPE_F32: torch.float32}
+
+
+class Dims(ctypes.Structure):
+    """Mirror of ``gdn_replay_dims``."""
+    _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("dk", ctypes.c_int32),
+                ("dv", ctypes.c_int32), ("T", ctypes.c_int32), ("cap", ctypes.c_int32),
+                ("threshold", ctypes.c_int32), ("n_slot", ctypes.c_int32),
+                ("in_dtype", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+    def __repr__(self):
+        return "Dims(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
+
+
+class GdnError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn} failed: {code} ({gdn_replay_strerror(code)})")
+        self.code = code
+
+
+_lib = None
+
+
+def load(rebuild: bool = False) -> ctypes.CDLL:
+    """Build (if stale) and load libgdnreplay.so; raises if that is impossible."""
+    global _lib
+    if _lib is None or rebuild:
+        path = _build.build(force=rebuild)
+        if not os.path.exists(path):
+            raise RuntimeError(f"libgdnreplay not found at {path}")
+        lib = ctypes.CDLL(path)
+        P, I = ctypes.c_void_p, ctypes.c_int32
+        D = ctypes.POINTER(Dims)
+        lib.gdn_replay_verify.argtypes = [D] + [P] * 15
+        lib.gdn_replay_accept.argtypes = [D, P, P, P, P, P]
+        lib.gdn_replay_flush.argtypes = [D] + [P] * 7 + [I, P, P]
+        lib.gdn_replay_strerror.argtypes = [ctypes.c_int]
+        lib.gdn_replay_strerror.restype = ctypes.c_char_p
+        lib.gdn_replay_version.argtypes = []
+        for f in (lib.gdn_replay_verify, lib.gdn_replay_accept, lib.gdn_replay_flush,
+                  lib.gdn_replay_version):
+            f.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def gdn_replay_strerror(code: int) -> str:
+    return load().gdn_replay_strerror(int(code)).decode()
+
+
+def _ptr(t, dtype=None, name=""):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, rc):
+    if rc != 0:
+        raise GdnError(fn, rc)
+
+
+def gdn_replay_verify(d: Dims, state, state_idx, buf_k, buf_v, buf_g, buf_beta, buf_len,
+                      q, k, v, g, beta, out, status, stream=None):
+    tin = _TORCH_IN.get(d.in_dtype)
+    f32, i32 = torch.float32, torch.int32
+    rc = load().gdn_replay_verify(
+        ctypes.byref(d), _ptr(state, f32, "state"), _ptr(state_idx, i32, "state_idx"),
+        _ptr(buf_k, tin, "buf_k"), _ptr(buf_v, tin, "buf_v"), _ptr(buf_g, f32, "buf_g"),
+        _ptr(buf_beta, f32, "buf_beta"), _ptr(buf_len, i32, "buf_len"),
+        _ptr(q, tin, "q"), _ptr(k, tin, "k"), _ptr(v, tin, "v"), _ptr(g, f32, "g"),
+        _ptr(beta, f32, "beta"), _ptr(out, f32, "out"), _ptr(status, i32, "status"),
+        _stream(stream))
+    _check("gdn_replay_verify", rc)
+
+
+def gdn_replay_accept(d: Dims, buf_len, state_idx, accepted, status, stream=None):
+    i32 = torch.int32
+    rc = load().gdn_replay_accept(ctypes.byref(d), _ptr(buf_len, i32, "buf_len"),
+                                  _ptr(state_idx, i32, "state_idx"),
+                                  _ptr(accepted, i32, "accepted"), _ptr(status, i32, "status"),
+                                  _stream(stream))
+    _check("gdn_replay_accept", rc)
+
+
+def gdn_replay_flush(d: Dims, state, state_idx, buf_k, buf_v, buf_g, buf_beta, buf_len, force,
+                     status, stream=None):
+    tin = _TORCH_IN.get(d.in_dtype)
+    f32, i32 = torch.float32, torch.int32
+    rc = load().gdn_replay_flush(
+        ctypes.byref(d), _ptr(state, f32, "state"), _ptr(state_idx, i32, "state_idx"),
+        _ptr(buf_k, tin, "buf_k"), _ptr(buf_v, tin, "buf_v"), _ptr(buf_g, f32, "buf_g"),
+        _ptr(buf_beta, f32, "buf_beta"), _ptr(buf_len, i32, "buf_len"), int(bool(force)),
+        _ptr(status, i32, "status"), _stream(stream))
+    _check("gdn_replay_flush", rc)
+
+
+class ReplayLayer:
+    """Device-resident checkpoint, buffer and lengths of one GDN layer.
+
+    ``init`` is a dict of CPU tensors with the layouts of ``include/gdnreplay.h``
+    (state, state_idx, buf_k, buf_v, buf_g, buf_beta, buf_len); they are copied
+    to ``device`` once.  The three methods enqueue the library calls.
+    """
+
+    def __init__(self, dims: Dims, init: dict, device="cuda"):
+        self.d = dims
+        self.t = {n: init[n].to(device).contiguous() for n in
+                  ("state", "state_idx", "buf_k", "buf_v", "buf_g", "buf_beta", "buf_len")}
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def verify(self, q, k, v, g, beta, out, stream=None):
+        t = self.t
+        gdn_replay_verify(self.d, t["state"], t["state_idx"], t["buf_k"], t["buf_v"], t["buf_g"],
+                          t["buf_beta"], t["buf_len"], q, k, v, g, beta, out, self.status, stream)
+
+    def accept(self, accepted, stream=None):
+        gdn_replay_accept(self.d, self.t["buf_len"], self.t["state_idx"], accepted, self.status,
+                          stream)
+
+    def flush(self, force=False, stream=None):
+        t = self.t
+        gdn_replay_flush(self.d, t["state"], t["state_idx"], t["buf_k"], t["buf_v"], t["buf_g"],
+                         t["buf_beta"], t["buf_len"], force, self.status, stream)

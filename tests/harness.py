@@ -1,0 +1,99 @@
+"""Shared test plumbing: run the CUDA library and the CPU oracle side by side
+on the same seeded inputs and compare them.
+
+Tolerance (floating point): per tensor and per (layer, step),
+    max |gpu - ref| <= 2e-3 * max |ref| + 1e-5
+with the fp64 oracle as ref.  Integer state (buffer lengths, status words)
+and the bytes copied into the buffer must match exactly.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+
+RTOL_MAX, ATOL = 2e-3, 1e-5
+
+
+def gpu_dims(wl: synth.Workload, B=None, n_slot=None):
+    import speculative_decode_recurrent_gb300 as lib
+    B = wl.B if B is None else B
+    return lib.Dims(B=B, H=wl.H, dk=wl.dk, dv=wl.dv, T=wl.T, cap=wl.cap, threshold=wl.threshold,
+                    n_slot=(B + max(1, B // 4)) if n_slot is None else n_slot,
+                    in_dtype=lib.DTYPE_BF16 if wl.in_dtype == "bf16" else lib.DTYPE_F32,
+                    scale=wl.scale)
+
+
+def oracle_dims(wl: synth.Workload, B=None, n_slot=None, threads=8):
+    B = wl.B if B is None else B
+    return oracle.Dims(B=B, H=wl.H, dk=wl.dk, dv=wl.dv, T=wl.T, cap=wl.cap, threshold=wl.threshold,
+                       n_slot=(B + max(1, B // 4)) if n_slot is None else n_slot,
+                       scale=wl.scale, n_threads=threads)
+
+
+def assert_close(name, got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{name}: non-finite values"
+    err = float(np.max(np.abs(got - ref))) if got.size else 0.0
+    bound = RTOL_MAX * (float(np.max(np.abs(ref))) if ref.size else 0.0) + ATOL
+    assert err <= bound, f"{name}: max|d|={err:.3e} > bound {bound:.3e}"
+    return err, bound
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().double().numpy()
+
+
+class Pair:
+    """GPU layer and oracle layer built from the same seeded initial state."""
+
+    def __init__(self, wl: synth.Workload, layer=0, B=None, device="cuda"):
+        import speculative_decode_recurrent_gb300 as lib
+        self.wl, self.layer = wl, layer
+        self.B = wl.B if B is None else B
+        init = synth.initial_layer(wl, layer, B=self.B)
+        self.gd = gpu_dims(wl, self.B)
+        self.od = oracle_dims(wl, self.B)
+        self.gpu = lib.ReplayLayer(self.gd, init, device)
+        self.orc = oracle.Layer(self.od, init)
+        self.device = device
+
+    def block(self, step):
+        return synth.draft_block(self.wl, self.layer, step, B=self.B)
+
+    def step(self, step, force=None, check=True, accepted=None):
+        """One verify -> accept -> flush on both sides; compares out, lengths,
+        status, and (after the flush) state and buffer."""
+        wl = self.wl
+        blk = self.block(step)
+        acc = blk["accepted"] if accepted is None else torch.as_tensor(accepted, dtype=torch.int32)
+        force = wl.forced_flush if force is None else force
+        dev = {n: blk[n].to(self.device) for n in ("q", "k", "v", "g", "beta")}
+        out = torch.empty(self.B, wl.T, wl.H, wl.dv, dtype=torch.float32, device=self.device)
+        self.gpu.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], out)
+        o_ref = self.orc.verify(blk)
+        self.gpu.accept(acc.to(self.device))
+        self.orc.accept(acc.numpy())
+        self.gpu.flush(force=force)
+        self.orc.flush(force=force)
+        torch.cuda.synchronize()
+        if check:
+            self.compare(out, o_ref, step)
+        return out, o_ref, acc
+
+    def compare(self, out, o_ref, step):
+        t = self.gpu.t
+        tag = f"layer{self.layer}/step{step}"
+        np.testing.assert_array_equal(t["buf_len"].cpu().numpy(), self.orc.buf_len, err_msg=tag)
+        assert int(self.gpu.status.item()) == int(self.orc.status[0]), tag
+        assert_close(f"out {tag}", to_np(out), o_ref)
+        assert_close(f"state {tag}", to_np(t["state"]), self.orc.state)
+        # the buffer holds copies of inputs: bit-exact
+        np.testing.assert_array_equal(to_np(t["buf_k"]), self.orc.buf_k, err_msg=tag)
+        np.testing.assert_array_equal(to_np(t["buf_v"]), self.orc.buf_v, err_msg=tag)
+        np.testing.assert_array_equal(to_np(t["buf_g"]), self.orc.buf_g, err_msg=tag)
+        np.testing.assert_array_equal(to_np(t["buf_beta"]), self.orc.buf_beta, err_msg=tag)

@@ -1,0 +1,98 @@
+"""The C-ABI library builds, loads and exports every declared symbol, and its
+host-side validation rejects bad arguments before anything is launched.
+No test here launches a kernel, so they all run without a GPU."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import speculative_decode_recurrent_gb300 as lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(gdn_[a-z0-9_]+)\s*\(",
+                             src, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("gdn_replay_verify", "gdn_replay_accept", "gdn_replay_flush", "gdn_replay_strerror"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    so = lib.load()
+    for n in declared_functions():
+        assert hasattr(so, n), f"missing export {n}"
+
+
+def test_dims_struct_layout():
+    assert ctypes.sizeof(lib.Dims) == 40
+    assert lib.Dims.scale.offset == 36
+
+
+def good_dims(**kw):
+    d = dict(B=2, H=2, dk=128, dv=128, T=4, cap=8, threshold=4, n_slot=2, in_dtype=lib.DTYPE_BF16,
+             scale=128 ** -0.5)
+    d.update(kw)
+    return lib.Dims(**d)
+
+
+FAKE = ctypes.c_void_p(0x10000)   # never dereferenced: validation fails first
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dk=96), -2), (dict(dv=32), -2), (dict(T=0), -2), (dict(T=65), -2),
+    (dict(cap=3), -2), (dict(cap=257), -2), (dict(threshold=0), -2), (dict(threshold=9), -2),
+    (dict(n_slot=1), -2), (dict(H=0), -2), (dict(B=-1), -2), (dict(in_dtype=7), -3),
+])
+def test_bad_dims_rejected_before_launch(kw, code):
+    so = lib.load()
+    d = good_dims(**kw)
+    assert so.gdn_replay_verify(ctypes.byref(d), *([FAKE] * 14), None) == code
+    assert so.gdn_replay_accept(ctypes.byref(d), FAKE, None, FAKE, FAKE, None) == code
+    assert so.gdn_replay_flush(ctypes.byref(d), *([FAKE] * 7), 0, FAKE, None) == code
+
+
+def test_null_pointers_rejected():
+    so = lib.load()
+    d = good_dims()
+    assert so.gdn_replay_verify(None, *([FAKE] * 14), None) == -1
+    for i in (0, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13):   # index 1 (state_idx) may be NULL
+        args = [FAKE] * 14
+        args[i] = None
+        assert so.gdn_replay_verify(ctypes.byref(d), *args, None) == -1, i
+    assert so.gdn_replay_accept(ctypes.byref(d), None, None, FAKE, FAKE, None) == -1
+    assert so.gdn_replay_accept(ctypes.byref(d), FAKE, None, None, FAKE, None) == -1
+    assert so.gdn_replay_flush(ctypes.byref(d), None, *([FAKE] * 6), 0, FAKE, None) == -1
+
+
+def test_misaligned_pointers_rejected():
+    so = lib.load()
+    d = good_dims()
+    args = [FAKE] * 14
+    args[0] = ctypes.c_void_p(0x10004)      # state must be 16-byte aligned
+    assert so.gdn_replay_verify(ctypes.byref(d), *args, None) == -2
+
+
+def test_empty_batch_is_a_noop():
+    so = lib.load()
+    d = good_dims(B=0, n_slot=0)
+    assert so.gdn_replay_verify(ctypes.byref(d), *([None] * 14), None) == 0
+    assert so.gdn_replay_accept(ctypes.byref(d), None, None, None, None, None) == 0
+    assert so.gdn_replay_flush(ctypes.byref(d), *([None] * 7), 1, None, None) == 0
+
+
+def test_strerror():
+    for c in (0, -1, -2, -3, -4, -99):
+        assert isinstance(lib.gdn_replay_strerror(c), str)

@@ -1,0 +1,257 @@
+"""GPU parity: libgdnreplay (through its C ABI) against the CPU oracle on the
+same seeded inputs.  Outputs and flushed state within
+max|d| <= 2e-3 max|ref| + 1e-5 per tensor per (layer, step); lengths, status
+words and buffer contents bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from harness import Pair, assert_close, to_np
+
+pytestmark = pytest.mark.gpu
+WL = synth.WORKLOADS
+
+
+@pytest.fixture(autouse=True)
+def _gpu(cuda_ok):
+    yield
+
+
+def test_tiny_verify_accept_forced_flush():
+    """The tiny workload: B=1, H=2, d=64, T=4, fp32 inputs, 3 buffered tokens,
+    one verify, a seeded accept in [0, 4], then a forced flush."""
+    Pair(WL["tiny"]).step(0)
+
+
+@pytest.mark.parametrize("p", [0, 1, 2, 3, 4])
+def test_tiny_every_accept_count(p):
+    Pair(WL["tiny"]).step(0, accepted=[p])
+
+
+def test_b8_multistep():
+    pr = Pair(WL["b8"])
+    for s in range(12):
+        pr.step(s)
+
+
+def test_edge_multistep_extreme_gates_and_forced_accepts():
+    """Forced accepts {0,1,8,15,16}, g in {0,-20}, beta near 0 and 1, threshold 64."""
+    pr = Pair(WL["edge"])
+    for s in range(12):
+        pr.step(s)
+
+
+@pytest.mark.parametrize("layer", [0, 23])
+def test_decode24_layers_first_and_last(layer):
+    pr = Pair(WL["decode24"], layer=layer)
+    for s in range(6):
+        pr.step(s)
+
+
+def test_large_batch_sampled_rows():
+    """B=128, H=32, T=8 on the GPU at full size; the oracle recomputes a
+    sample of the sequences (they are independent) for every checked tensor."""
+    wl = WL["large"]
+    import speculative_decode_recurrent_gb300 as lib
+    init = synth.initial_layer(wl, 0)
+    from harness import gpu_dims, oracle_dims
+    gd = gpu_dims(wl)
+    gpu = lib.ReplayLayer(gd, init)
+    sample = np.array([0, 1, 37, 64, 100, 127])
+    sub = dict(init)
+    sub["state_idx"] = init["state_idx"][sample]
+    od = oracle_dims(wl, B=len(sample), n_slot=gd.n_slot)
+    orc = oracle.Layer(od, sub)
+    for s in range(3):
+        blk = synth.draft_block(wl, 0, s)
+        dev = {n: blk[n].cuda() for n in ("q", "k", "v", "g", "beta")}
+        out = torch.empty(wl.B, wl.T, wl.H, wl.dv, device="cuda")
+        gpu.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], out)
+        sblk = {n: blk[n][sample] for n in ("q", "k", "v", "g", "beta")}
+        o_ref = orc.verify(sblk)
+        gpu.accept(blk["accepted"].cuda())
+        orc.accept(blk["accepted"][sample].numpy())
+        gpu.flush()
+        orc.flush()
+        torch.cuda.synchronize()
+        assert_close(f"out step{s}", to_np(out)[sample], o_ref)
+        slots = init["state_idx"][sample].long().numpy()
+        assert_close(f"state step{s}", to_np(gpu.t["state"])[slots], orc.state[slots])
+        np.testing.assert_array_equal(gpu.t["buf_len"].cpu().numpy()[slots], orc.buf_len[slots])
+        assert int(gpu.status.item()) == 0
+
+
+# ------------------------------------------------------------ exact invariants
+def _one_verify(pr, step=0):
+    wl = pr.wl
+    blk = pr.block(step)
+    dev = {n: blk[n].cuda() for n in ("q", "k", "v", "g", "beta")}
+    out = torch.empty(pr.B, wl.T, wl.H, wl.dv, device="cuda")
+    pr.gpu.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], out)
+    return out, blk
+
+
+def test_verify_is_pure_and_repeatable():
+    pr = Pair(WL["b8"])
+    st0 = pr.gpu.t["state"].clone()
+    ln0 = pr.gpu.t["buf_len"].clone()
+    o1, _ = _one_verify(pr)
+    o2, _ = _one_verify(pr)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
+    assert torch.equal(pr.gpu.t["state"], st0)
+    assert torch.equal(pr.gpu.t["buf_len"], ln0)
+
+
+def test_full_rejection_is_bit_identical():
+    pr = Pair(WL["b8"])
+    t = pr.gpu.t
+    st0, ln0, bk0 = t["state"].clone(), t["buf_len"].clone(), t["buf_k"].clone()
+    _one_verify(pr)
+    pr.gpu.accept(torch.zeros(pr.B, dtype=torch.int32, device="cuda"))
+    pr.gpu.flush(force=False)
+    torch.cuda.synchronize()
+    assert torch.equal(t["state"], st0)
+    assert torch.equal(t["buf_len"], ln0)
+    for s in range(t["buf_len"].numel()):
+        L = int(ln0[s])
+        assert torch.equal(t["buf_k"][s, :, :L], bk0[s, :, :L])
+    assert int(pr.gpu.status.item()) == 0
+
+
+def test_flush_empty_noop_and_idempotent():
+    pr = Pair(WL["b8"])
+    t = pr.gpu.t
+    t["buf_len"].zero_()
+    st0 = t["state"].clone()
+    pr.gpu.flush(force=True)
+    torch.cuda.synchronize()
+    assert torch.equal(t["state"], st0)
+    t["buf_len"].fill_(5)
+    pr.gpu.flush(force=True)
+    torch.cuda.synchronize()
+    st1 = t["state"].clone()
+    assert (t["buf_len"][pr.gpu.t["state_idx"].long()] == 0).all()
+    pr.gpu.flush(force=True)
+    torch.cuda.synchronize()
+    assert torch.equal(t["state"], st1)
+
+
+def test_status_bits_without_trap():
+    """Bad accepted counts and a full buffer are reported in the status word;
+    the affected sequences are skipped and nothing traps."""
+    pr = Pair(WL["b8"])
+    t = pr.gpu.t
+    idx = t["state_idx"].long()
+    t["buf_len"][idx[0]] = pr.wl.cap - pr.wl.T + 1          # no room for the draft
+    out, _ = _one_verify(pr)
+    torch.cuda.synchronize()
+    assert int(pr.gpu.status.item()) == 2
+    pr.gpu.status.zero_()
+    ln0 = t["buf_len"].clone()
+    acc = torch.tensor([-1, pr.wl.T + 1] + [0] * (pr.B - 2), dtype=torch.int32, device="cuda")
+    pr.gpu.accept(acc)
+    torch.cuda.synchronize()
+    assert int(pr.gpu.status.item()) == 1
+    assert torch.equal(t["buf_len"], ln0)
+    pr.gpu.status.zero_()
+    t["buf_len"][idx[1]] = pr.wl.cap + 3                    # corrupt length
+    pr.gpu.flush(force=False)
+    torch.cuda.synchronize()
+    assert int(pr.gpu.status.item()) & 4
+
+
+def test_guard_bands_untouched():
+    """Every written tensor gets a NaN tail; the kernels must never touch it."""
+    import speculative_decode_recurrent_gb300 as lib
+    wl = WL["edge"]
+    init = synth.initial_layer(wl, 0)
+    from harness import gpu_dims
+    d = gpu_dims(wl)
+    pad = 4096
+
+    def padded(t):
+        flat = torch.full((t.numel() + pad,), float("nan"), dtype=t.dtype, device="cuda") \
+            if t.dtype.is_floating_point else torch.full((t.numel() + pad,), -7, dtype=t.dtype,
+                                                          device="cuda")
+        flat[:t.numel()] = t.reshape(-1).cuda()
+        return flat, flat[:t.numel()].view(t.shape)
+
+    names = ("state", "buf_k", "buf_v", "buf_g", "buf_beta", "buf_len")
+    store = {n: padded(init[n]) for n in names}
+    t = {n: store[n][1] for n in names}
+    t["state_idx"] = init["state_idx"].cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for s in range(4):
+        blk = synth.draft_block(wl, 0, s)
+        out_flat, out = padded(torch.zeros(wl.B, wl.T, wl.H, wl.dv))
+        dev = {n: blk[n].cuda() for n in ("q", "k", "v", "g", "beta")}
+        lib.gdn_replay_verify(d, t["state"], t["state_idx"], t["buf_k"], t["buf_v"], t["buf_g"],
+                              t["buf_beta"], t["buf_len"], dev["q"], dev["k"], dev["v"], dev["g"],
+                              dev["beta"], out, status)
+        lib.gdn_replay_accept(d, t["buf_len"], t["state_idx"], blk["accepted"].cuda(), status)
+        lib.gdn_replay_flush(d, t["state"], t["state_idx"], t["buf_k"], t["buf_v"], t["buf_g"],
+                             t["buf_beta"], t["buf_len"], 0, status)
+        torch.cuda.synchronize()
+        assert torch.isnan(out_flat[out.numel():].float()).all()
+        for n in names:
+            tail = store[n][0][init[n].numel():]
+            if tail.dtype.is_floating_point:
+                assert torch.isnan(tail.float()).all(), n
+            else:
+                assert (tail == -7).all(), n
+    assert int(status.item()) == 0
+
+
+def test_default_stream_and_side_stream_agree():
+    pr1, pr2 = Pair(WL["b8"]), Pair(WL["b8"])
+    o1, _ = _one_verify(pr1)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o2, _ = _one_verify(pr2)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
+
+
+def test_checkpoint_resume_bit_identical():
+    """State + buffer + lengths are the resumable unit: saving them to the host
+    and restoring them continues bit-identically."""
+    import speculative_decode_recurrent_gb300 as lib
+    wl = WL["b8"]
+    init = synth.initial_layer(wl, 0)
+    from harness import gpu_dims
+    d = gpu_dims(wl)
+    a = lib.ReplayLayer(d, init)
+    for s in range(3):
+        _step_layer(a, wl, s)
+    snap = {n: v.cpu().clone() for n, v in a.t.items()}
+    b = lib.ReplayLayer(d, snap)
+    for s in range(3, 6):
+        oa = _step_layer(a, wl, s)
+        ob = _step_layer(b, wl, s)
+        torch.cuda.synchronize()
+        assert torch.equal(oa, ob)
+    for n in a.t:
+        assert torch.equal(a.t[n], b.t[n]), n
+
+
+def _step_layer(layer, wl, s):
+    blk = synth.draft_block(wl, 0, s)
+    dev = {n: blk[n].cuda() for n in ("q", "k", "v", "g", "beta")}
+    out = torch.empty(wl.B, wl.T, wl.H, wl.dv, device="cuda")
+    layer.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], out)
+    layer.accept(blk["accepted"].cuda())
+    layer.flush()
+    return out
+
+
+def test_bad_slot_reported_not_dereferenced():
+    pr = Pair(WL["b8"])
+    pr.gpu.t["state_idx"][3] = pr.gd.n_slot + 100
+    _one_verify(pr)
+    pr.gpu.accept(torch.zeros(pr.B, dtype=torch.int32, device="cuda"))
+    pr.gpu.flush(force=True)
+    torch.cuda.synchronize()
+    assert int(pr.gpu.status.item()) == 8
