@@ -75,6 +75,7 @@ typedef struct CUstream_st *cudaStream_t;
 #define GDN_STATUS_NO_ROOM    2   /* verify: buf_len + T > cap; b skipped */
 #define GDN_STATUS_BAD_LEN    4   /* buf_len outside [0, cap] (accept: len + p > cap); b skipped */
 #define GDN_STATUS_BAD_SLOT   8   /* state_idx[b] outside [0, n_slot); b skipped */
+#define GDN_STATUS_TIMEOUT   16   /* a bounded on-chip wait expired; the (b, h) unit was skipped */
 
 typedef struct {
     int32_t B;          /* batch rows (sequences) in this call, >= 0 */

@@ -12,8 +12,8 @@ import sys
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SOURCES = [os.path.join(PKG, "csrc", "gdn_replay.cu")]
-HEADERS = [os.path.join(ROOT, "include", "gdnreplay.h")]
+SOURCES = [os.path.join(PKG, "csrc", f) for f in ("gdn_replay.cu", "gdn_replay_tc.cu")]
+HEADERS = [os.path.join(ROOT, "include", "gdnreplay.h"), os.path.join(PKG, "csrc", "replay_common.h")]
 LIB = os.path.join(PKG, "_build", "libgdnreplay.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -33,15 +33,26 @@ def stale() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile every translation unit in parallel, then link the shared library."""
     if not force and not stale():
         return LIB
-    os.makedirs(os.path.dirname(LIB), exist_ok=True)
-    tmp = LIB + f".{os.getpid()}.tmp"
-    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
-           "-I", os.path.join(ROOT, "include"), "-o", tmp, *SOURCES]
+    out = os.path.dirname(LIB)
+    os.makedirs(out, exist_ok=True)
+    common = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+              "-I", os.path.join(ROOT, "include")]
     if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    subprocess.check_call(cmd)
+        common.append("-Xptxas=-v")
+    objs, procs = [], []
+    for src in SOURCES:
+        obj = os.path.join(out, os.path.basename(src) + f".{os.getpid()}.o")
+        objs.append(obj)
+        procs.append(subprocess.Popen(common + ["-c", src, "-o", obj]))
+    if any(p.wait() != 0 for p in procs):
+        raise RuntimeError("nvcc failed while building libgdnreplay")
+    tmp = LIB + f".{os.getpid()}.tmp"
+    subprocess.check_call([nvcc(), *ARCH, "-shared", "-o", tmp, *objs])
+    for o in objs:
+        os.remove(o)
     os.replace(tmp, LIB)
     return LIB
 

@@ -27,9 +27,11 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
-#include "gdnreplay.h"
+#include "replay_common.h"
 
 namespace {
+
+using gdn::ReplayArgs;
 
 constexpr int kRows = 64;               // state rows per CTA
 constexpr float kRenorm = 5.421011e-20f;  // 2^-64
@@ -55,20 +57,6 @@ template <> struct InVec<float> {
     }
 };
 
-struct ReplayArgs {
-    const float *state_in;      // verify: checkpoint (read)
-    float *state_out;           // flush: checkpoint (read + write)
-    const int32_t *state_idx;
-    void *buf_k, *buf_v;
-    float *buf_g, *buf_beta;
-    const int32_t *buf_len;
-    const void *q, *k, *v;
-    const float *g, *beta;
-    float *out;
-    int32_t *status;
-    int B, H, T, cap, threshold, force, n_slot;
-    float scale;
-};
 
 // Copy `n` token rows of width D (elements of TIn) into fp32 shared memory,
 // rows [dst0, dst0 + n).  Token r comes from src + r * src_stride.  When
@@ -194,7 +182,7 @@ __device__ __forceinline__ void replay_pertoken(const ReplayArgs &a)
         const float acc = row_sum<TPR>((acc4.x + acc4.y) + (acc4.z + acc4.w));   // (St k_t)_row
         c *= sa[t];                                      // c' = a_t c
         const float w = sb[t] * (sv[(size_t)t * DV + row] - c * acc);
-        const float coef = w / c;
+        const float coef = __fdividef(w, c);
 #pragma unroll
         for (int m = 0; m < NC; ++m) {                   // keys re-read from shared memory
             const float4 kv = kt[TPR * m + part];
@@ -329,6 +317,8 @@ int gdn_replay_verify(const gdn_replay_dims *d, const float *state, const int32_
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = out; a.status = status;
     a.B = d->B; a.H = d->H; a.T = d->T; a.cap = d->cap; a.threshold = d->threshold;
     a.n_slot = d->n_slot; a.scale = d->scale;
+    const int tc = gdn::tc_verify(d, a, stream);
+    if (tc <= 0) return tc;
     return dispatch_replay<true>(d, a, stream);
 }
 
@@ -361,7 +351,8 @@ int gdn_replay_flush(const gdn_replay_dims *d, float *state, const int32_t *stat
     a.buf_len = buf_len; a.status = status;
     a.B = d->B; a.H = d->H; a.T = d->T; a.cap = d->cap; a.threshold = d->threshold;
     a.force = force ? 1 : 0; a.n_slot = d->n_slot; a.scale = d->scale;
-    int r = dispatch_replay<false>(d, a, stream);
+    int r = gdn::tc_flush(d, a, stream);
+    if (r > 0) r = dispatch_replay<false>(d, a, stream);
     if (r) return r;
     flush_lengths_kernel<<<(d->B + 127) / 128, 128, 0, stream>>>(buf_len, state_idx, d->B, d->n_slot,
                                                                   d->cap, d->threshold, a.force, status);

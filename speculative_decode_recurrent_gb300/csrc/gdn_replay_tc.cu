@@ -90,6 +90,22 @@ __device__ __forceinline__ void mma_tf32(uint32_t d, uint64_t a, uint64_t b, uin
         ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int x, int y, const void *src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(saddr(src))
+                 : "memory");
+}
+__device__ __forceinline__ void tma_store_commit_and_wait() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(bar))
                  : "memory");
@@ -144,10 +160,11 @@ __host__ __device__ inline int round16(int x) { return (x + 15) & ~15; }
 //   [64K, 64K + SB)    [K;Q] fp32 tile, 4 sub-tiles of NP rows x 128 B, plus
 //                      slack so an M=128 operand may read past row NP;
 //                      after the MMAs: the coefficient matrices (row stride CP+4)
-//   then: 2 mbarriers, TMEM slot, flag, G (hi, lo), beta, gamma per token.
+//   then: 2 mbarriers, TMEM slot, flag, and G (hi, lo), beta, gamma per token, each
+//   array padded to a multiple of 16 tokens so it can be read as float4.
 __host__ __device__ inline int verify_sb_bytes(int cap, int T) { return (3 * round16(cap + T) + 128) * 128; }
 __host__ __device__ inline int verify_smem_bytes(int cap, int T) {
-    return 1024 + 65536 + verify_sb_bytes(cap, T) + 64 + 16 * (cap + T);
+    return 1024 + 65536 + verify_sb_bytes(cap, T) + 64 + 16 * round16(cap + T);
 }
 
 template <int CMAX>
@@ -179,10 +196,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm);            // [0] TMA, [1] MMA
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + 16);
     int *flag = reinterpret_cast<int *>(sm + 20);
+    const int GS = round16(cap + T);                              // per-token array stride (16-B rows)
     float *sGh = reinterpret_cast<float *>(sm + 64);
-    float *sGl = sGh + (cap + T);
-    float *sBeta = sGl + (cap + T);
-    float *sGam = sBeta + (cap + T);
+    float *sGl = sGh + GS;
+    float *sBeta = sGl + GS;
+    float *sGam = sBeta + GS;
     float *sMat = reinterpret_cast<float *>(sB);                  // reused after the MMAs
     float *sR = reinterpret_cast<float *>(sA);                    // reused after the MMAs: [C][128]
     float *sPQ = sR + static_cast<size_t>(C) * 128;               //                        [T][128]
@@ -207,7 +225,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
         for (int kb = 0; kb < 4; ++kb) tma_load_2d(sA + kb * 16384, &tm_state, kb * 32, y, &bar[0]);
     }
 
-    // ---- keys (buffer, draft) and queries -> fp32 swizzled tile; draft -> buffer
+    // ---- every global load of this unit, issued back to back (one memory latency)
     const __nv_bfloat16 *bk = reinterpret_cast<const __nv_bfloat16 *>(a.buf_k) + unit * cap * 128;
     const __nv_bfloat16 *bv = reinterpret_cast<const __nv_bfloat16 *>(a.buf_v) + unit * cap * 128;
     const size_t drow0 = (static_cast<size_t>(b) * T * H + h) * 128;   // draft token 0 of (b, h)
@@ -217,71 +235,121 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     const __nv_bfloat16 *dv = reinterpret_cast<const __nv_bfloat16 *>(a.v) + drow0;
     __nv_bfloat16 *wk = reinterpret_cast<__nv_bfloat16 *>(a.buf_k) + (unit * cap + len) * 128;
     __nv_bfloat16 *wv = reinterpret_cast<__nv_bfloat16 *>(a.buf_v) + (unit * cap + len) * 128;
-    for (int e = tid; e < (C + T) * 16; e += kThreads) {
-        const int r = e >> 4, c = e & 15;                         // token row, 8-element vector
-        const __nv_bfloat16 *src = r < len ? bk + static_cast<size_t>(r) * 128
-                                 : r < C   ? dk + static_cast<size_t>(r - len) * dstride
-                                           : dq + static_cast<size_t>(r - C) * dstride;
-        const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(src) + c);
-        if (r >= len && r < C) reinterpret_cast<uint4 *>(wk + static_cast<size_t>(r - len) * 128)[c] = raw;
-        float f[8];
-        bf16x8_to_f32(raw, f);
-        uint8_t *tile = sB + (c >> 2) * NP * 128;
-        const int ch = (c & 3) * 2;
-        *reinterpret_cast<float4 *>(tile + sw128(r, ch)) = make_float4(f[0], f[1], f[2], f[3]);
-        *reinterpret_cast<float4 *>(tile + sw128(r, ch + 1)) = make_float4(f[4], f[5], f[6], f[7]);
-    }
-    for (int e = tid; e < T * 16; e += kThreads) {
-        const int r = e >> 4, c = e & 15;
-        reinterpret_cast<uint4 *>(wv + static_cast<size_t>(r) * 128)[c] =
-            __ldg(reinterpret_cast<const uint4 *>(dv + static_cast<size_t>(r) * dstride) + c);
-    }
-    for (int t = tid; t < C; t += kThreads) {
-        float gg, be;
-        if (t < len) {
-            gg = a.buf_g[unit * cap + t];
-            be = a.buf_beta[unit * cap + t];
-        } else {
-            const size_t gi = (static_cast<size_t>(b) * T + (t - len)) * H + h;
-            gg = a.g[gi];
-            be = a.beta[gi];
-            a.buf_g[unit * cap + t] = gg;
-            a.buf_beta[unit * cap + t] = be;
+    constexpr int NV = (CMAX + 16) * 16 / kThreads;               // 16-byte vectors of [K;Q] per thread
+    uint4 raw[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+        if (r < C + T) {
+            const __nv_bfloat16 *src = r < len ? bk + static_cast<size_t>(r) * 128
+                                     : r < C   ? dk + static_cast<size_t>(r - len) * dstride
+                                               : dq + static_cast<size_t>(r - C) * dstride;
+            raw[i] = __ldg(reinterpret_cast<const uint4 *>(src) + c);
         }
-        sGh[t] = gg;
-        sBeta[t] = be;
     }
-    // value channel `tid` of every replayed token, gathered early (independent of the MMA)
-    float vr[CMAX];
+    uint4 rawv[2];                                                // draft values, staged to the buffer
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+        if (r < T) rawv[i] = __ldg(reinterpret_cast<const uint4 *>(dv + static_cast<size_t>(r) * dstride) + c);
+    }
+    // value channel `tid` of every token: unconditional loads from clamped addresses so
+    // that all of them are in flight together; widened to fp32 only when first used
+    unsigned short vraw[CMAX];
 #pragma unroll
     for (int t = 0; t < CMAX; ++t) {
-        vr[t] = 0.f;
-        if (t < C) {
-            const __nv_bfloat16 *vp = t < len ? bv + static_cast<size_t>(t) * 128
-                                              : dv + static_cast<size_t>(t - len) * dstride;
-            vr[t] = __bfloat162float(vp[tid]);
+        const int tc = t < C ? t : C - 1;
+        const __nv_bfloat16 *vp = tc < len ? bv + static_cast<size_t>(tc) * 128
+                                           : dv + static_cast<size_t>(tc - len) * dstride;
+        vraw[t] = __ldg(reinterpret_cast<const unsigned short *>(vp) + tid);
+    }
+    float gq[2] = {0.f, 0.f}, bq[2] = {0.f, 0.f};                 // gates of tokens lane, lane + 32 (warp 0)
+    if (warp == 0) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int t = (tid & 31) + 32 * i;
+            if (t < C) {
+                if (t < len) {
+                    gq[i] = a.buf_g[unit * cap + t];
+                    bq[i] = a.buf_beta[unit * cap + t];
+                } else {
+                    const size_t gi = (static_cast<size_t>(b) * T + (t - len)) * H + h;
+                    gq[i] = a.g[gi];
+                    bq[i] = a.beta[gi];
+                }
+            }
+        }
+    }
+    // ---- widen [K;Q] into the swizzled fp32 tile; draft k, v, g, beta -> buffer
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+        if (r < C + T) {
+            if (r >= len && r < C) reinterpret_cast<uint4 *>(wk + static_cast<size_t>(r - len) * 128)[c] = raw[i];
+            float f[8];
+            bf16x8_to_f32(raw[i], f);
+            uint8_t *tile = sB + (c >> 2) * NP * 128;
+            const int ch = (c & 3) * 2;
+            *reinterpret_cast<float4 *>(tile + sw128(r, ch)) = make_float4(f[0], f[1], f[2], f[3]);
+            *reinterpret_cast<float4 *>(tile + sw128(r, ch + 1)) = make_float4(f[4], f[5], f[6], f[7]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+        if (r < T) reinterpret_cast<uint4 *>(wv + static_cast<size_t>(r) * 128)[c] = rawv[i];
+    }
+    if (warp == 0) {
+        // running log-decay G_t = sum_{s<=t} g_s as a compensated pair (hi + lo): a
+        // Kogge-Stone scan with two-sum steps over tokens lane and lane + 32
+        const int lane = tid & 31;
+        float hi[2], lo[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            hi[i] = gq[i];
+            lo[i] = 0.f;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float h2 = __shfl_up_sync(0xffffffffu, hi[i], off);
+                const float l2 = __shfl_up_sync(0xffffffffu, lo[i], off);
+                if (lane >= off) {
+                    const float s1 = hi[i] + h2, bp = s1 - hi[i];
+                    lo[i] += l2 + ((hi[i] - (s1 - bp)) + (h2 - bp));
+                    hi[i] = s1;
+                }
+            }
+        }
+        const float ch = __shfl_sync(0xffffffffu, hi[0], 31), cl = __shfl_sync(0xffffffffu, lo[0], 31);
+        {
+            const float s1 = hi[1] + ch, bp = s1 - hi[1];
+            lo[1] += cl + ((hi[1] - (s1 - bp)) + (ch - bp));
+            hi[1] = s1;
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int t = lane + 32 * i;
+            if (t < C) {
+                sGh[t] = hi[i];
+                sGl[t] = lo[i];
+                sGam[t] = __expf(hi[i] + lo[i]);
+                sBeta[t] = bq[i];
+                if (t >= len) {
+                    a.buf_g[unit * cap + t] = gq[i];
+                    a.buf_beta[unit * cap + t] = bq[i];
+                }
+            }
         }
     }
     fence_proxy_async();                      // generic writes of the [K;Q] tile -> async proxy
     __syncthreads();
-    if (tid == 0) {                           // running log-decay, compensated (G = hi + lo)
-        float hi = 0.f, lo = 0.f;
-        for (int t = 0; t < C; ++t) {
-            const float g = sGh[t];
-            const float s = hi + g, bp = s - hi;
-            lo += (hi - (s - bp)) + (g - bp);
-            hi = s;
-            sGh[t] = hi;
-            sGl[t] = lo;
-            sGam[t] = __expf(hi + lo);
-        }
+    if (tid == 0) {
         if (mbar_wait(&bar[0], 0)) {
             tc_fence_after();
             const uint32_t idP = idesc_mn(2, 128, NP), idK = idesc_mn(2, 128, CP);
             const uint32_t a0 = saddr(sA), b0 = saddr(sB);
 #pragma unroll
             for (int ks = 0; ks < 16; ++ks) {                      // K = 128 in steps of 8 (32 bytes)
-                const uint32_t off = (ks >> 2) * 0u + (ks & 3) * 32;
+                const uint32_t off = (ks & 3) * 32;
                 mma_tf32(tmem, desc_sw128(a0 + (ks >> 2) * 16384 + off),
                          desc_sw128(b0 + (ks >> 2) * NP * 128 + off), idP, ks > 0);
             }
@@ -323,12 +391,20 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
             const int p = is_q ? len + (tid - C) : tid;          // position of this row's token
             const float gh = sGh[p], gl = sGl[p];
             const float scl = is_q ? 1.f : sBeta[tid];
+            const int lim = is_q ? min(p + 1, C) : tid;           // columns s < lim are used
+            float gs[16], ls[16];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float4 x = *reinterpret_cast<const float4 *>(sGh + c0 + 4 * j);
+                const float4 y = *reinterpret_cast<const float4 *>(sGl + c0 + 4 * j);
+                gs[4 * j] = x.x; gs[4 * j + 1] = x.y; gs[4 * j + 2] = x.z; gs[4 * j + 3] = x.w;
+                ls[4 * j] = y.x; ls[4 * j + 1] = y.y; ls[4 * j + 2] = y.z; ls[4 * j + 3] = y.w;
+            }
             float m[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const int s = c0 + j;
-                const bool use = is_q ? (s <= p && s < C) : (s < tid);
-                m[j] = use ? scl * __expf((gh - sGh[s]) + (gl - sGl[s])) * kq[j] : 0.f;
+                const float e = __expf((gh - gs[j]) + (gl - ls[j]));
+                m[j] = (c0 + j < lim) ? scl * e * kq[j] : 0.f;
             }
             float4 *dst = reinterpret_cast<float4 *>(sMat + static_cast<size_t>(tid) * LDA + c0);
 #pragma unroll
@@ -336,26 +412,35 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
         }
     }
     // ---- right-hand sides rhs_t = beta_t (v_t - gamma_t (S0 k_t)) and the S0 q columns
-    for (int c0 = 0; c0 < NP; c0 += 16) {
+#pragma unroll
+    for (int c0 = 0; c0 < CMAX; c0 += 16) {                       // key columns [0, C)
+        if (c0 >= C) break;
         float pc[16];
         tmem_ld16(lane_base + c0, pc);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             const int t = c0 + j;
-            if (t < C) {
-                float vt = 0.f;
+            if (t < C)
+                sR[static_cast<size_t>(t) * 128 + tid] =
+                    sBeta[t] * (__bfloat162float(__ushort_as_bfloat16(vraw[t])) - sGam[t] * pc[j]);
+        }
+    }
+    for (int c0 = C & ~15; c0 < C + T; c0 += 16) {                // query columns [C, C+T)
+        float pc[16];
+        tmem_ld16(lane_base + c0, pc);
 #pragma unroll
-                for (int s = 0; s < CMAX; ++s) vt = (s == t) ? vr[s] : vt;
-                sR[static_cast<size_t>(t) * 128 + tid] = sBeta[t] * (vt - sGam[t] * pc[j]);
-            } else if (t < C + T) {
-                sPQ[static_cast<size_t>(t - C) * 128 + tid] = pc[j];
-            }
+        for (int j = 0; j < 16; ++j) {
+            const int t = c0 + j;
+            if (t >= C && t < C + T) sPQ[static_cast<size_t>(t - C) * 128 + tid] = pc[j];
         }
     }
     __syncthreads();
 
-    // ---- forward substitution, one state row per thread
+    // ---- forward substitution, one state row per thread.  Coefficient rows hold zeros
+    // at s >= t and u[s] is zero until assigned, so whole 4-wide groups need no guards.
     float u[CMAX];
+#pragma unroll
+    for (int t = 0; t < CMAX; ++t) u[t] = 0.f;
 #pragma unroll
     for (int t = 0; t < CMAX; ++t) {
         if (t >= C) break;
@@ -365,31 +450,380 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
         for (int s = 0; s < t; s += 4) {
             const float4 a4 = *reinterpret_cast<const float4 *>(Ar + s);
             c0 = fmaf(a4.x, u[s], c0);
-            if (s + 1 < t) c1 = fmaf(a4.y, u[s + 1], c1);
-            if (s + 2 < t) c2 = fmaf(a4.z, u[s + 2], c2);
-            if (s + 3 < t) c3 = fmaf(a4.w, u[s + 3], c3);
+            c1 = fmaf(a4.y, u[s + 1], c1);
+            c2 = fmaf(a4.z, u[s + 2], c2);
+            c3 = fmaf(a4.w, u[s + 3], c3);
         }
         u[t] = sR[static_cast<size_t>(t) * 128 + tid] - ((c0 + c1) + (c2 + c3));
     }
-    // ---- draft outputs o_t = scale (gamma_p S0 q_t + sum_{s<=p} e^{G_p-G_s} (q_t.k_s) u_s)
+    // ---- draft outputs o_t = scale (gamma_p S0 q_t + sum_{s<=p} e^{G_p-G_s} (q_t.k_s) u_s);
+    // the coefficient rows are zero past p and past C, so every row sums over [0, CP)
     for (int t2 = 0; t2 < T; ++t2) {
         const int p = len + t2;
         const float *Mr = sMat + static_cast<size_t>(C + t2) * LDA;
         float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
 #pragma unroll
         for (int s = 0; s < CMAX; s += 4) {
-            if (s > p) break;
+            if ((s & 15) == 0 && s >= CP) break;
             const float4 m4 = *reinterpret_cast<const float4 *>(Mr + s);
             c0 = fmaf(m4.x, u[s], c0);
-            if (s + 1 <= p) c1 = fmaf(m4.y, u[s + 1], c1);
-            if (s + 2 <= p) c2 = fmaf(m4.z, u[s + 2], c2);
-            if (s + 3 <= p) c3 = fmaf(m4.w, u[s + 3], c3);
+            c1 = fmaf(m4.y, u[s + 1], c1);
+            c2 = fmaf(m4.z, u[s + 2], c2);
+            c3 = fmaf(m4.w, u[s + 3], c3);
         }
         const float o = sGam[p] * sPQ[static_cast<size_t>(t2) * 128 + tid] + ((c0 + c1) + (c2 + c3));
         a.out[((static_cast<size_t>(b) * T + t2) * H + h) * 128 + tid] = a.scale * o;
     }
 
     tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Three bf16 terms whose sum is x exactly (for normal-range x): each rounding
+// to bf16 keeps the next 8-9 significant bits of what is left.
+__device__ __forceinline__ void split3(float x, __nv_bfloat16 &h, __nv_bfloat16 &m, __nv_bfloat16 &l) {
+    h = __float2bfloat16_rn(x);
+    const float r1 = x - __bfloat162float(h);
+    m = __float2bfloat16_rn(r1);
+    l = __float2bfloat16_rn(r1 - __bfloat162float(m));
+}
+__device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
+    return static_cast<uint32_t>(__bfloat16_as_ushort(a)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
+}
+
+// Shared-memory plan of the flush kernel (bytes from the 1024-aligned base):
+//   [0, 64K)      S0 tile, fp32, TMA-loaded; rewritten with the new state and TMA-stored
+//   [64K, 160K)   S0 as three bf16 tiles (128 x 128 each, 2 sub-tiles of 128 B rows);
+//                 after the first MMAs: U~ as three bf16 tiles [64K, 112K), K^T bf16
+//                 [112K, 128K) and the coefficient matrix [128K, 160K)
+//   [160K, 192K)  K, bf16, 2 sub-tiles of 128 rows x 128 B (rows >= C unused)
+//   then: 2 mbarriers, TMEM slot, flag, G (hi, lo), beta, gamma per token.
+__host__ __device__ inline int flush_smem_bytes(int cap) { return 1024 + 196608 + 64 + 16 * round16(cap); }
+
+template <int CMAX>
+__global__ void __launch_bounds__(kThreads, 1)
+flush_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
+{
+    const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+    const int slot = a.state_idx ? a.state_idx[b] : b;
+    if (slot < 0 || slot >= a.n_slot) return;                      // reported by the length kernel
+    const int len = a.buf_len[slot];
+    const int H = a.H, cap = a.cap;
+    if (len < 0 || len > cap) return;                               // reported by the length kernel
+    if (!(len >= a.threshold || (a.force && len > 0))) return;
+    const int C = len;
+    const int CP = round16(C);
+    const int LDA = CP + 4;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sS = base;
+    uint8_t *sX = base + 65536;
+    uint8_t *sU = sX;                                               // 3 x 16 KB after the first MMAs
+    uint8_t *sKt = sX + 49152;                                      // 16 KB
+    float *sMat = reinterpret_cast<float *>(sX + 65536);            // <= 32 KB
+    uint8_t *sK = base + 163840;
+    uint8_t *sm = base + 196608;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + 16);
+    int *flag = reinterpret_cast<int *>(sm + 20);
+    const int GS = round16(cap);                                   // per-token array stride (16-B rows)
+    float *sGh = reinterpret_cast<float *>(sm + 64);
+    float *sGl = sGh + GS;
+    float *sBeta = sGl + GS;
+    float *sGam = sBeta + GS;
+
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        *flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const size_t unit = static_cast<size_t>(slot) * H + h;
+    const int y = static_cast<int>(unit) * 128;
+    if (tid == 0) {
+        mbar_expect_tx(&bar[0], 65536);
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) tma_load_2d(sS + kb * 16384, &tm_state, kb * 32, y, &bar[0]);
+    }
+    // keys of the buffered tokens (bf16, copied as is into the swizzled K tile), the
+    // value channel `tid` of every token and the gates: all loads issued back to back
+    const __nv_bfloat16 *bk = reinterpret_cast<const __nv_bfloat16 *>(a.buf_k) + unit * cap * 128;
+    const __nv_bfloat16 *bv = reinterpret_cast<const __nv_bfloat16 *>(a.buf_v) + unit * cap * 128;
+    constexpr int NV = CMAX * 16 / kThreads;
+    uint4 raw[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+        if (r < C) raw[i] = __ldg(reinterpret_cast<const uint4 *>(bk + static_cast<size_t>(r) * 128) + c);
+    }
+    unsigned short vraw[CMAX];                                      // clamped, unconditional loads
+#pragma unroll
+    for (int t = 0; t < CMAX; ++t)
+        vraw[t] = __ldg(reinterpret_cast<const unsigned short *>(bv + static_cast<size_t>(t < C ? t : C - 1) * 128) + tid);
+    float gq[2] = {0.f, 0.f}, bq[2] = {0.f, 0.f};
+    if (warp == 0) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int t = (tid & 31) + 32 * i;
+            if (t < C) {
+                gq[i] = a.buf_g[unit * cap + t];
+                bq[i] = a.buf_beta[unit * cap + t];
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+        if (r < C) *reinterpret_cast<uint4 *>(sK + (c >> 3) * 16384 + sw128(r, c & 7)) = raw[i];
+    }
+    if (warp == 0) {                                                // compensated scan of g (see verify)
+        const int lane = tid & 31;
+        float hi[2], lo[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            hi[i] = gq[i];
+            lo[i] = 0.f;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float h2 = __shfl_up_sync(0xffffffffu, hi[i], off);
+                const float l2 = __shfl_up_sync(0xffffffffu, lo[i], off);
+                if (lane >= off) {
+                    const float s1 = hi[i] + h2, bp = s1 - hi[i];
+                    lo[i] += l2 + ((hi[i] - (s1 - bp)) + (h2 - bp));
+                    hi[i] = s1;
+                }
+            }
+        }
+        const float ch = __shfl_sync(0xffffffffu, hi[0], 31), cl = __shfl_sync(0xffffffffu, lo[0], 31);
+        {
+            const float s1 = hi[1] + ch, bp = s1 - hi[1];
+            lo[1] += cl + ((hi[1] - (s1 - bp)) + (ch - bp));
+            hi[1] = s1;
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int t = lane + 32 * i;
+            if (t < C) {
+                sGh[t] = hi[i];
+                sGl[t] = lo[i];
+                sGam[t] = __expf(hi[i] + lo[i]);
+                sBeta[t] = bq[i];
+            }
+        }
+    }
+    if (tid == 0 && !mbar_wait(&bar[0], 0)) *flag = 1;
+    __syncthreads();
+    if (*flag) {
+        if (tid == 0) {
+            mbar_wait(&bar[0], 0);
+            atomicOr(a.status, kStatusTimeout);
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+        return;
+    }
+    // ---- S0 row `tid` -> three bf16 tiles (exact split)
+    {
+        const int r = tid;
+#pragma unroll 4
+        for (int c8 = 0; c8 < 16; ++c8) {                           // 8 columns per step
+            const float4 x0 = *reinterpret_cast<const float4 *>(sS + (c8 >> 2) * 16384 + sw128(r, (c8 & 3) * 2));
+            const float4 x1 = *reinterpret_cast<const float4 *>(sS + (c8 >> 2) * 16384 + sw128(r, (c8 & 3) * 2 + 1));
+            const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            __nv_bfloat16 hh[8], mm[8], ll[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) split3(xs[j], hh[j], mm[j], ll[j]);
+            const uint32_t off = (c8 >> 3) * 16384 + sw128(r, c8 & 7);
+            *reinterpret_cast<uint4 *>(sX + off) =
+                make_uint4(pack2(hh[0], hh[1]), pack2(hh[2], hh[3]), pack2(hh[4], hh[5]), pack2(hh[6], hh[7]));
+            *reinterpret_cast<uint4 *>(sX + 32768 + off) =
+                make_uint4(pack2(mm[0], mm[1]), pack2(mm[2], mm[3]), pack2(mm[4], mm[5]), pack2(mm[6], mm[7]));
+            *reinterpret_cast<uint4 *>(sX + 65536 + off) =
+                make_uint4(pack2(ll[0], ll[1]), pack2(ll[2], ll[3]), pack2(ll[4], ll[5]), pack2(ll[6], ll[7]));
+        }
+    }
+    fence_proxy_async();
+    __syncthreads();
+    if (tid == 0) {
+        tc_fence_after();
+        const uint32_t idP = idesc_mn(1, 128, CP);
+        const uint32_t x0 = saddr(sX), k0 = saddr(sK);
+#pragma unroll
+        for (int sp = 0; sp < 3; ++sp)
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {                        // K = 128 in steps of 16 (32 bytes)
+                const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                mma_bf16(tmem, desc_sw128(x0 + sp * 32768 + off), desc_sw128(k0 + off), idP, (sp | ks) != 0);
+            }
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            const uint64_t d = desc_sw128(k0 + off);
+            mma_bf16(tmem + CP, d, d, idP, ks > 0);
+        }
+        mma_commit(&bar[1]);
+    }
+    bool ok = mbar_wait(&bar[1], 0);
+    if (__syncthreads_or(!ok)) {
+        if (tid == 0) {
+            mbar_wait(&bar[1], 0);
+            atomicOr(a.status, kStatusTimeout);
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+        return;
+    }
+    tc_fence_after();
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    // ---- coefficient rows A[t][s] = beta_t e^{G_t-G_s} (k_t.k_s), s < t
+    for (int c0 = 0; c0 < CP; c0 += 16) {
+        float kq[16];
+        tmem_ld16(lane_base + CP + c0, kq);
+        if (tid < C) {
+            const float gh = sGh[tid], gl = sGl[tid], be = sBeta[tid];
+            float gs[16], ls[16];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float4 x = *reinterpret_cast<const float4 *>(sGh + c0 + 4 * j);
+                const float4 y = *reinterpret_cast<const float4 *>(sGl + c0 + 4 * j);
+                gs[4 * j] = x.x; gs[4 * j + 1] = x.y; gs[4 * j + 2] = x.z; gs[4 * j + 3] = x.w;
+                ls[4 * j] = y.x; ls[4 * j + 1] = y.y; ls[4 * j + 2] = y.z; ls[4 * j + 3] = y.w;
+            }
+            float m[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float e = __expf((gh - gs[j]) + (gl - ls[j]));
+                m[j] = (c0 + j < tid) ? be * e * kq[j] : 0.f;
+            }
+            float4 *dst = reinterpret_cast<float4 *>(sMat + static_cast<size_t>(tid) * LDA + c0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dst[j] = make_float4(m[4 * j], m[4 * j + 1], m[4 * j + 2], m[4 * j + 3]);
+        }
+    }
+    __syncthreads();
+    // ---- forward substitution for state row `tid`
+    float u[CMAX];
+    float pc[16];
+#pragma unroll
+    for (int t = 0; t < CMAX; ++t) u[t] = 0.f;
+#pragma unroll
+    for (int t = 0; t < CMAX; ++t) {
+        if (t >= C) break;
+        if ((t & 15) == 0) tmem_ld16(lane_base + t, pc);
+        const float *Ar = sMat + static_cast<size_t>(t) * LDA;
+        float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+#pragma unroll
+        for (int s = 0; s < t; s += 4) {                            // zeros at s >= t (see verify)
+            const float4 a4 = *reinterpret_cast<const float4 *>(Ar + s);
+            c0 = fmaf(a4.x, u[s], c0);
+            c1 = fmaf(a4.y, u[s + 1], c1);
+            c2 = fmaf(a4.z, u[s + 2], c2);
+            c3 = fmaf(a4.w, u[s + 3], c3);
+        }
+        const float vt = __bfloat162float(__ushort_as_bfloat16(vraw[t]));
+        u[t] = sBeta[t] * (vt - sGam[t] * pc[t & 15]) - ((c0 + c1) + (c2 + c3));
+    }
+    // ---- U~ = e^{G_C - G_s} u_s as three bf16 tiles (row tid, K = token), and K^T
+    {
+        const float gh = sGh[C - 1], gl = sGl[C - 1];
+#pragma unroll
+        for (int c8 = 0; c8 < CMAX / 8; ++c8) {
+            __nv_bfloat16 hh[8], mm[8], ll[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int s = c8 * 8 + j;
+                const float w = s < C ? __expf((gh - sGh[s]) + (gl - sGl[s])) * u[s] : 0.f;
+                split3(w, hh[j], mm[j], ll[j]);
+            }
+            if (c8 * 8 < CP) {
+                const uint32_t off = sw128(tid, c8);
+                *reinterpret_cast<uint4 *>(sU + off) =
+                    make_uint4(pack2(hh[0], hh[1]), pack2(hh[2], hh[3]), pack2(hh[4], hh[5]), pack2(hh[6], hh[7]));
+                *reinterpret_cast<uint4 *>(sU + 16384 + off) =
+                    make_uint4(pack2(mm[0], mm[1]), pack2(mm[2], mm[3]), pack2(mm[4], mm[5]), pack2(mm[6], mm[7]));
+                *reinterpret_cast<uint4 *>(sU + 32768 + off) =
+                    make_uint4(pack2(ll[0], ll[1]), pack2(ll[2], ll[3]), pack2(ll[4], ll[5]), pack2(ll[6], ll[7]));
+            }
+        }
+        // K^T row `tid` (key channel j = tid): k_s[j] for s < CP, zero past C
+        const __nv_bfloat16 zero = __float2bfloat16_rn(0.f);
+        for (int c8 = 0; c8 < CP / 8; ++c8) {
+            __nv_bfloat16 kk[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int s = c8 * 8 + j;
+                kk[j] = s < C ? *reinterpret_cast<const __nv_bfloat16 *>(
+                                    sK + (tid >> 6) * 16384 + sw128(s, (tid & 63) >> 3) + (tid & 7) * 2)
+                              : zero;
+            }
+            *reinterpret_cast<uint4 *>(sKt + sw128(tid, c8)) =
+                make_uint4(pack2(kk[0], kk[1]), pack2(kk[2], kk[3]), pack2(kk[4], kk[5]), pack2(kk[6], kk[7]));
+        }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+        tc_fence_after();
+        const uint32_t idF = idesc_mn(1, 128, 128);
+        const uint32_t u0 = saddr(sU), kt0 = saddr(sKt);
+        for (int sp = 0; sp < 3; ++sp)
+            for (int ks = 0; ks < CP / 16; ++ks)
+                mma_bf16(tmem, desc_sw128(u0 + sp * 16384 + ks * 32), desc_sw128(kt0 + ks * 32), idF,
+                         (sp | ks) != 0);
+        mma_commit(&bar[1]);
+    }
+    ok = mbar_wait(&bar[1], 1);
+    if (__syncthreads_or(!ok)) {
+        if (tid == 0) {
+            mbar_wait(&bar[1], 1);
+            atomicOr(a.status, kStatusTimeout);
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+        return;
+    }
+    tc_fence_after();
+    // ---- S_C = gamma_C S0 + D, written over the S0 tile, then one TMA store
+    {
+        const float gC = sGam[C - 1];
+        const int r = tid;
+#pragma unroll 2
+        for (int c0 = 0; c0 < 128; c0 += 16) {
+            float d[16];
+            tmem_ld16(lane_base + c0, d);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int col = c0 + 4 * q;                          // 4 fp32 = one 16-byte chunk
+                float4 *p = reinterpret_cast<float4 *>(sS + (col >> 5) * 16384 + sw128(r, (col & 31) >> 2));
+                float4 x = *p;
+                x.x = fmaf(gC, x.x, d[4 * q]);
+                x.y = fmaf(gC, x.y, d[4 * q + 1]);
+                x.z = fmaf(gC, x.z, d[4 * q + 2]);
+                x.w = fmaf(gC, x.w, d[4 * q + 3]);
+                *p = x;
+            }
+        }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) tma_store_2d(&tm_state, kb * 32, y, sS + kb * 16384);
+        tma_store_commit_and_wait();
+    }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
@@ -436,13 +870,24 @@ int launch_verify(const gdn_replay_dims *d, const ReplayArgs &a, const CUtensorM
 
 int tc_verify(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s) {
     if (d->dk != 128 || d->dv != 128 || d->in_dtype != GDN_DTYPE_BF16) return 1;
-    if (d->cap > 80 || d->cap + d->T > 128) return 1;
+    if (d->cap > 64 || d->T > 16) return 1;                       // C <= 64 tokens, T <= 16 queries
     if (verify_smem_bytes(d->cap, d->T) > 227 * 1024) return 1;
     CUtensorMap m;
     if (!state_map(&m, a.state_in, d->n_slot * d->H * 128)) return 1;
-    return d->cap <= 48 ? launch_verify<48>(d, a, m, s) : launch_verify<80>(d, a, m, s);
+    return d->cap <= 48 ? launch_verify<48>(d, a, m, s) : launch_verify<64>(d, a, m, s);
 }
 
-int tc_flush(const gdn_replay_dims *, const ReplayArgs &, cudaStream_t) { return 1; }
+int tc_flush(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s) {
+    if (d->dk != 128 || d->dv != 128 || d->in_dtype != GDN_DTYPE_BF16) return 1;
+    if (d->cap > 64 || flush_smem_bytes(d->cap) > 227 * 1024) return 1;
+    CUtensorMap m;
+    if (!state_map(&m, a.state_out, d->n_slot * d->H * 128)) return 1;
+    const int smem = flush_smem_bytes(d->cap);
+    auto kern = d->cap <= 48 ? flush_tc_kernel<48> : flush_tc_kernel<64>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return GDN_ERR_LAUNCH;
+    kern<<<dim3(d->H, d->B), kThreads, smem, s>>>(m, a);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+}
 
 }  // namespace gdn

@@ -27,7 +27,7 @@ struct ReplayArgs {
 
 // Internal status bit: a bounded wait in a tensor-core kernel gave up (the
 // affected unit is skipped; nothing hangs).
-constexpr int32_t kStatusTimeout = 16;
+constexpr int32_t kStatusTimeout = GDN_STATUS_TIMEOUT;
 
 // Tensor-core path (gdn_replay_tc.cu).  Each returns GDN_OK when it launched,
 // GDN_ERR_LAUNCH on a launch failure, and 1 when the shape is not one it
