@@ -38,7 +38,7 @@ ACCEPT_PERIOD = 16      # distinct accepted-count patterns, cycled over steps
 FALLBACK_HBM_GBS = 6800.0
 # dram read+write bytes per verify launch from the ncu capture summarised in
 # profiles/; valid only for the kernel source whose hash is recorded with it.
-NCU_TRAFFIC = {}        # {source_sha1: bytes_per_launch}
+NCU_TRAFFIC = {}        # {(step mode, source_sha1): bytes_per_launch}
 
 
 def parse():
@@ -72,6 +72,18 @@ def bytes_model(wl, lens_before, acc):
     flush = H * (2 * st * fl.sum() + tok_buf * new[fl].sum()) + len(L) * 8
     new2 = np.where(fl, 0, new)
     return verify, accept, flush, new2, int(new[fl].sum())
+
+
+def bytes_model_fused(wl, lens_before, acc):
+    """Algorithmic bytes of one fused layer-step (verify_fold + accept_fold): the
+    verify traffic, plus one state write per (sequence, head) whose buffer is folded.
+    Returns (verify_fold, accept, new_lens, n_folded_sequences)."""
+    verify, accept, _, _, _ = bytes_model(wl, lens_before, np.zeros_like(acc))
+    L = lens_before.astype(np.int64)
+    fold = L >= wl.threshold
+    verify += wl.H * wl.dv * wl.dk * 4 * int(fold.sum())
+    new = np.where(fold, 0, L) + acc.astype(np.int64)
+    return verify, accept, new, int(fold.sum())
 
 
 def clocks_sampler():
@@ -130,7 +142,8 @@ def hbm_peak():
 
 def source_sha1():
     h = hashlib.sha1()
-    for rel in ("speculative_decode_recurrent_gb300/csrc/gdn_replay.cu",):
+    for rel in ("speculative_decode_recurrent_gb300/csrc/gdn_replay.cu",
+                "speculative_decode_recurrent_gb300/csrc/gdn_replay_tc.cu"):
         h.update(open(os.path.join(ROOT, rel), "rb").read())
     return h.hexdigest()
 
@@ -164,7 +177,7 @@ def _accept_pattern(wl, layer, j):
 
 
 # ------------------------------------------------------------------- GPU run
-def run_ours(args, rank, world):
+def run_ours(args, rank, world, mode="fused"):
     import speculative_decode_recurrent_gb300 as lib
 
     wl = synth.WORKLOADS[WORKLOAD]
@@ -190,18 +203,27 @@ def run_ours(args, rank, world):
     outs = [torch.empty(wl.B, wl.T, wl.H, wl.dv, device=dev) for _ in range(L)]
     stream = torch.cuda.Stream(device=dev)
 
+    fused = mode == "fused"
+
     def enqueue_step(j, events=None):
         for l in range(L):
             blk = pools[l][j % DRAFT_POOL]
             if events is not None:
                 events[l][0].record()
-            layers[l].verify(blk["q"], blk["k"], blk["v"], blk["g"], blk["beta"], outs[l])
+            if fused:
+                layers[l].verify_fold(blk["q"], blk["k"], blk["v"], blk["g"], blk["beta"], outs[l])
+            else:
+                layers[l].verify(blk["q"], blk["k"], blk["v"], blk["g"], blk["beta"], outs[l])
             if events is not None:
                 events[l][1].record()
-            layers[l].accept(acc_dev[l][j])
+            if fused:
+                layers[l].accept_fold(acc_dev[l][j])
+            else:
+                layers[l].accept(acc_dev[l][j])
             if events is not None:
                 events[l][2].record()
-            layers[l].flush(force=False)
+            if not fused:
+                layers[l].flush(force=False)
             if events is not None:
                 events[l][3].record()
 
@@ -218,12 +240,20 @@ def run_ours(args, rank, world):
     lens = [x.copy() for x in lens0]
     tot = {"verify": 0, "accept": 0, "flush": 0, "tokens": 0}
 
+    def step_bytes(l, j):
+        if fused:
+            v, a, new, _ = bytes_model_fused(wl, lens[l], acc_host[l][j])
+            f = 0
+        else:
+            v, a, f, new, _ = bytes_model(wl, lens[l], acc_host[l][j])
+        lens[l] = new
+        return v, a, f
+
     def account(j):
         for l in range(L):
-            v, a, f, new, _ = bytes_model(wl, lens[l], acc_host[l][j])
+            v, a, f = step_bytes(l, j)
             tot["verify"] += v; tot["accept"] += a; tot["flush"] += f
             tot["tokens"] += int(acc_host[l][j].sum())
-            lens[l] = new
 
     for s in range(args.warmup):
         graphs[s % ACCEPT_PERIOD].replay()
@@ -282,10 +312,11 @@ def run_ours(args, rank, world):
                 per_k["verify"].append(evs[l][0].elapsed_time(evs[l][1]))
                 per_k["accept"].append(evs[l][1].elapsed_time(evs[l][2]))
                 per_k["flush"].append(evs[l][2].elapsed_time(evs[l][3]))
-                v, a, f, new, _ = bytes_model(wl, lens[l], acc_host[l][j])
+                v, a, f = step_bytes(l, j)
                 kb["verify"] += v; kb["flush"] += f
-                lens[l] = new
         kern_ms = {k: float(np.mean(v)) for k, v in per_k.items()}
+        if fused:
+            kern_ms.pop("flush")
         verify_bytes_per_launch = kb["verify"] / (n_inst * L)
         flush_bytes_per_launch = kb["flush"] / (n_inst * L)
     except TypeError:
@@ -305,9 +336,13 @@ def run_ours(args, rank, world):
             with torch.cuda.graph(ge, stream=stream):
                 for l in range(L):
                     b = stage[l]
-                    layers[l].verify(b["q"], b["k"], b["v"], b["g"], b["beta"], outs[l])
-                    layers[l].accept(acc_stage[l])
-                    layers[l].flush(force=False)
+                    if fused:
+                        layers[l].verify_fold(b["q"], b["k"], b["v"], b["g"], b["beta"], outs[l])
+                        layers[l].accept_fold(acc_stage[l])
+                    else:
+                        layers[l].verify(b["q"], b["k"], b["v"], b["g"], b["beta"], outs[l])
+                        layers[l].accept(acc_stage[l])
+                        layers[l].flush(force=False)
         h2d = sum(sum(t.numel() * t.element_size() for n, t in pin[l].items() if n != "accepted")
                   + acc_pin[l].numel() * 4 for l in range(L))
         d2h = sum(o.numel() * o.element_size() for o in outs)
@@ -334,8 +369,13 @@ def run_ours(args, rank, world):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": args.e2e_steps}
 
+    launches_per_step = (2 if fused else 4) * L
+    del graphs, layers, pools
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     return dict(ms=ms, clocks=clocks, timed_bytes=timed_bytes, kern_ms=kern_ms,
-                verify_bpl=verify_bytes_per_launch, flush_bpl=flush_bytes_per_launch, e2e=e2e, L=L)
+                verify_bpl=verify_bytes_per_launch, flush_bpl=flush_bytes_per_launch, e2e=e2e, L=L,
+                launches_per_step=launches_per_step, mode=mode)
 
 
 def main():
@@ -378,44 +418,60 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device(
             "cuda", int(os.environ.get("LOCAL_RANK", 0))))
-    r = run_ours(args, rank, world)
+    r3 = run_ours(args, rank, world, mode="three_call")
+    r = run_ours(args, rank, world, mode="fused")
     if rank == 0:
-        L = r["L"]
-        us_layer = r["ms"] * 1000.0 / (args.steps * L * world)
-        tb = r["timed_bytes"]
-        total_bytes = tb["verify"] + tb["accept"] + tb["flush"]
-        gbs = total_bytes / (r["ms"] * 1e-3) / 1e9 * world
         peak, peak_kind = hbm_peak()
-        roof = None
-        if r["kern_ms"]:
-            ach = r["verify_bpl"] / (r["kern_ms"]["verify"] * 1e-3) / 1e9
-            traffic = NCU_TRAFFIC.get(source_sha1())
-            roof = {"bound": "hbm", "kernel": "verify", "achieved": round(ach, 1),
-                    "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
-                    "peak_source": f"{peak_kind} HBM copy bandwidth",
-                    "traffic": traffic,
-                    "algorithmic_bytes_per_launch": int(r["verify_bpl"]),
-                    "kernel_us": {k: round(v * 1000.0, 3) for k, v in r["kern_ms"].items()},
-                    "flush_achieved_gbs": round(r["flush_bpl"] / (r["kern_ms"]["flush"] * 1e-3) / 1e9, 1)}
+
+        def summary(rr):
+            L = rr["L"]
+            tb = rr["timed_bytes"]
+            total_bytes = tb["verify"] + tb["accept"] + tb["flush"]
+            out = {"us_per_layer": round(rr["ms"] * 1000.0 / (args.steps * L * world), 3),
+                   "hbm_gbs": round(total_bytes / (rr["ms"] * 1e-3) / 1e9 * world, 1),
+                   "algorithmic_bytes_per_step": int(total_bytes / args.steps),
+                   "tokens_per_s": round(tb["tokens"] / L / (rr["ms"] * 1e-3) * world, 1)}
+            out["hbm_frac"] = round(out["hbm_gbs"] / peak, 4)
+            roof = None
+            if rr["kern_ms"]:
+                ach = rr["verify_bpl"] / (rr["kern_ms"]["verify"] * 1e-3) / 1e9
+                roof = {"bound": "hbm", "kernel": "verify_fold" if rr["mode"] == "fused" else "verify",
+                        "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                        "frac": round(ach / peak, 4), "peak_source": f"{peak_kind} HBM copy bandwidth",
+                        "traffic": NCU_TRAFFIC.get((rr["mode"], source_sha1())),
+                        "algorithmic_bytes_per_launch": int(rr["verify_bpl"]),
+                        "kernel_us": {k: round(v * 1000.0, 3) for k, v in rr["kern_ms"].items()}}
+                if rr["mode"] != "fused":
+                    roof["flush_achieved_gbs"] = round(
+                        rr["flush_bpl"] / (rr["kern_ms"]["flush"] * 1e-3) / 1e9, 1)
+            return out, roof
+
+        s_f, roof_f = summary(r)
+        s_3, roof_3 = summary(r3)
         cpu = None
         if not args.no_cpu_baseline:
             el, n, threads, B = cpu_oracle_run(synth.WORKLOADS[WORKLOAD], args.cpu_seconds)
             cpu = {"value": round(el * 1e6 / n, 3), "unit": "us/layer", "cores": threads,
                    "kind": "oracle", "sample": f"layer 0, B={B}, {n} consecutive layer-steps "
                                                f"(~{args.cpu_seconds:.0f} s of fp64 C on host cores)"}
-        line = {"metric": metric, "value": round(us_layer, 3), "unit": "us/layer", "n_gpus": world,
+        line = {"metric": metric, "value": s_f["us_per_layer"], "unit": "us/layer", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": round(r["ms"] / args.steps, 4), "higher_is_better": False,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
                 "config": {"workload": workload_desc,
+                           "step": "fused: gdn_replay_verify_fold + gdn_replay_accept_fold per layer "
+                                   "(flush folded into the next verify)",
                            "l2": "inputs larger than L2 (24 layers x 33.5 MB state rotate per step)",
                            "parallelism": f"replicas x{world} (batch-sharded, no collective)",
                            "draft_pool": DRAFT_POOL, "accept_period": ACCEPT_PERIOD},
-                "tokens_per_s": round(tb["tokens"] / L / (r["ms"] * 1e-3) * world, 1),
-                "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4),
-                "algorithmic_bytes_per_step": int(total_bytes / args.steps),
-                "roofline": roof, "cpu_baseline": cpu, "e2e": r["e2e"],
-                "gpu_launches": 4 * L * args.steps, "clocks": r["clocks"]}
+                "tokens_per_s": s_f["tokens_per_s"], "hbm_gbs": s_f["hbm_gbs"],
+                "hbm_frac": s_f["hbm_frac"],
+                "algorithmic_bytes_per_step": s_f["algorithmic_bytes_per_step"],
+                "roofline": roof_f, "cpu_baseline": cpu, "e2e": r["e2e"],
+                "gpu_launches": r["launches_per_step"] * args.steps, "clocks": r["clocks"],
+                "three_call": dict(s_3, step="gdn_replay_verify + gdn_replay_accept + gdn_replay_flush",
+                                   roofline=roof_3, e2e=r3["e2e"], clocks=r3["clocks"],
+                                   gpu_launches=r3["launches_per_step"] * args.steps)}
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -135,6 +135,39 @@ int gdn_replay_flush(const gdn_replay_dims *dims, float *state,
                      int32_t *buf_len, int32_t force, int32_t *status,
                      cudaStream_t stream);
 
+/*
+ * Lazy flush -- the periodic flush folded into the next verify, so the
+ * checkpoint of a flushed sequence is read once instead of twice (the fusion
+ * the blog's section "Avoiding unnecessary memory transfers" argues for, applied
+ * to the flush of "Making speculative verification cheaper").  A decode step is
+ *     gdn_replay_verify_fold(...);  gdn_replay_accept_fold(...);
+ * and is equivalent to  gdn_replay_flush(force = 0); gdn_replay_verify; gdn_replay_accept.
+ *
+ * gdn_replay_verify_fold -- as gdn_replay_verify, except that a sequence whose
+ * len = buf_len[s] is >= threshold first has its len buffered tokens folded into
+ * state[s,h] (written in place, fp32) and its draft staged at buffer slots
+ * [0, T) instead of [len, len+T).  Outputs are those of verify after that fold.
+ * buf_len is NOT written (every head of a sequence reads the same len); the
+ * following gdn_replay_accept_fold applies the reset.  Requires
+ * threshold - 1 + T <= cap; lengths before the call may reach threshold - 1 + T.
+ */
+int gdn_replay_verify_fold(const gdn_replay_dims *dims,
+                           float *state, const int32_t *state_idx,
+                           void *buf_k, void *buf_v, float *buf_g, float *buf_beta,
+                           const int32_t *buf_len,
+                           const void *q, const void *k, const void *v,
+                           const float *g, const float *beta,
+                           float *out, int32_t *status, cudaStream_t stream);
+
+/*
+ * gdn_replay_accept_fold -- the accept that follows gdn_replay_verify_fold:
+ * buf_len[s] = (len >= threshold ? 0 : len) + accepted[b], with the checks of
+ * gdn_replay_accept.  Writes only buf_len.
+ */
+int gdn_replay_accept_fold(const gdn_replay_dims *dims, int32_t *buf_len,
+                           const int32_t *state_idx, const int32_t *accepted,
+                           int32_t *status, cudaStream_t stream);
+
 /* Human-readable text for a GDN_ERR_* code (static storage). */
 const char *gdn_replay_strerror(int code);
 

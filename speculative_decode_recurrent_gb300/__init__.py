@@ -16,11 +16,12 @@ import torch
 from . import build as _build
 
 __all__ = ["Dims", "GdnError", "load", "gdn_replay_verify", "gdn_replay_accept",
-           "gdn_replay_flush", "gdn_replay_strerror", "STATUS_BAD_ACCEPT", "STATUS_NO_ROOM",
-           "STATUS_BAD_LEN", "DTYPE_BF16", "DTYPE_F32", "ReplayLayer"]
+           "gdn_replay_flush", "gdn_replay_verify_fold", "gdn_replay_accept_fold",
+           "gdn_replay_strerror", "STATUS_BAD_ACCEPT", "STATUS_NO_ROOM", "STATUS_BAD_LEN",
+           "STATUS_BAD_SLOT", "STATUS_TIMEOUT", "DTYPE_BF16", "DTYPE_F32", "ReplayLayer"]
 
 DTYPE_BF16, DTYPE_F32 = 0, 1
-STATUS_BAD_ACCEPT, STATUS_NO_ROOM, STATUS_BAD_LEN, STATUS_BAD_SLOT = 1, 2, 4, 8
+STATUS_BAD_ACCEPT, STATUS_NO_ROOM, STATUS_BAD_LEN, STATUS_BAD_SLOT, STATUS_TIMEOUT = 1, 2, 4, 8, 16
 _TORCH_IN = {DTYPE_BF16: torch.bfloat16, DTYPE_F32: torch.float32}
 
 
@@ -57,11 +58,13 @@ def load(rebuild: bool = False) -> ctypes.CDLL:
         lib.gdn_replay_verify.argtypes = [D] + [P] * 15
         lib.gdn_replay_accept.argtypes = [D, P, P, P, P, P]
         lib.gdn_replay_flush.argtypes = [D] + [P] * 7 + [I, P, P]
+        lib.gdn_replay_verify_fold.argtypes = [D] + [P] * 15
+        lib.gdn_replay_accept_fold.argtypes = [D, P, P, P, P, P]
         lib.gdn_replay_strerror.argtypes = [ctypes.c_int]
         lib.gdn_replay_strerror.restype = ctypes.c_char_p
         lib.gdn_replay_version.argtypes = []
         for f in (lib.gdn_replay_verify, lib.gdn_replay_accept, lib.gdn_replay_flush,
-                  lib.gdn_replay_version):
+                  lib.gdn_replay_verify_fold, lib.gdn_replay_accept_fold, lib.gdn_replay_version):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -107,6 +110,29 @@ def gdn_replay_verify(d: Dims, state, state_idx, buf_k, buf_v, buf_g, buf_beta, 
         _ptr(beta, f32, "beta"), _ptr(out, f32, "out"), _ptr(status, i32, "status"),
         _stream(stream))
     _check("gdn_replay_verify", rc)
+
+
+def gdn_replay_verify_fold(d: Dims, state, state_idx, buf_k, buf_v, buf_g, buf_beta, buf_len,
+                           q, k, v, g, beta, out, status, stream=None):
+    tin = _TORCH_IN.get(d.in_dtype)
+    f32, i32 = torch.float32, torch.int32
+    rc = load().gdn_replay_verify_fold(
+        ctypes.byref(d), _ptr(state, f32, "state"), _ptr(state_idx, i32, "state_idx"),
+        _ptr(buf_k, tin, "buf_k"), _ptr(buf_v, tin, "buf_v"), _ptr(buf_g, f32, "buf_g"),
+        _ptr(buf_beta, f32, "buf_beta"), _ptr(buf_len, i32, "buf_len"),
+        _ptr(q, tin, "q"), _ptr(k, tin, "k"), _ptr(v, tin, "v"), _ptr(g, f32, "g"),
+        _ptr(beta, f32, "beta"), _ptr(out, f32, "out"), _ptr(status, i32, "status"),
+        _stream(stream))
+    _check("gdn_replay_verify_fold", rc)
+
+
+def gdn_replay_accept_fold(d: Dims, buf_len, state_idx, accepted, status, stream=None):
+    i32 = torch.int32
+    rc = load().gdn_replay_accept_fold(ctypes.byref(d), _ptr(buf_len, i32, "buf_len"),
+                                       _ptr(state_idx, i32, "state_idx"),
+                                       _ptr(accepted, i32, "accepted"), _ptr(status, i32, "status"),
+                                       _stream(stream))
+    _check("gdn_replay_accept_fold", rc)
 
 
 def gdn_replay_accept(d: Dims, buf_len, state_idx, accepted, status, stream=None):
@@ -157,3 +183,13 @@ class ReplayLayer:
         t = self.t
         gdn_replay_flush(self.d, t["state"], t["state_idx"], t["buf_k"], t["buf_v"], t["buf_g"],
                          t["buf_beta"], t["buf_len"], force, self.status, stream)
+
+    def verify_fold(self, q, k, v, g, beta, out, stream=None):
+        t = self.t
+        gdn_replay_verify_fold(self.d, t["state"], t["state_idx"], t["buf_k"], t["buf_v"],
+                               t["buf_g"], t["buf_beta"], t["buf_len"], q, k, v, g, beta, out,
+                               self.status, stream)
+
+    def accept_fold(self, accepted, stream=None):
+        gdn_replay_accept_fold(self.d, self.t["buf_len"], self.t["state_idx"], accepted,
+                               self.status, stream)

@@ -93,11 +93,18 @@ __host__ __device__ inline size_t replay_smem_floats(int dk, int dv, int cap, in
     return (size_t)cap * dk + (size_t)T * dk + (size_t)cap * dv + 2 * (size_t)cap;
 }
 
-// VERIFY = true : checkpoint + buffer + draft, outputs, stage draft into buffer.
-// VERIFY = false: flush; replay the buffer onto the checkpoint and store it.
-template <int DK, int DV, typename TIn, bool VERIFY>
+// MODE 0 (verify): checkpoint + buffer + draft, outputs, stage draft into buffer.
+// MODE 1 (flush):  replay the buffer onto the checkpoint and store it.
+// MODE 2 (verify with fold): as verify, and a unit whose buffer reached the
+//   threshold also stores the state after its buffered tokens and stages the
+//   draft at buffer slot 0 (one CTA owns all rows of the unit in this mode).
+enum { kVerify = 0, kFlush = 1, kVerifyFold = 2 };
+
+template <int DK, int DV, typename TIn, int MODE>
 __device__ __forceinline__ void replay_pertoken(const ReplayArgs &a)
 {
+    constexpr bool VERIFY = MODE != kFlush;
+    constexpr int ROWS = MODE == kVerifyFold ? DV : kRows;
     constexpr int TPR = DK / 16;                         // threads per state row
     extern __shared__ __align__(16) float smem[];
     const int h = blockIdx.x, b = blockIdx.y;
@@ -108,9 +115,11 @@ __device__ __forceinline__ void replay_pertoken(const ReplayArgs &a)
     }
     const int len = a.buf_len[slot];
     int n_tok;
+    const bool fold = MODE == kVerifyFold && len >= a.threshold && len <= a.cap;
     if (VERIFY) {
-        if (len < 0 || len + a.T > a.cap) {
-            if (threadIdx.x == 0 && h == 0 && blockIdx.z == 0) atomicOr(a.status, GDN_STATUS_NO_ROOM);
+        if (len < 0 || (!fold && len + a.T > a.cap)) {
+            if (threadIdx.x == 0 && h == 0 && blockIdx.z == 0)
+                atomicOr(a.status, len < 0 || len > a.cap ? GDN_STATUS_BAD_LEN : GDN_STATUS_NO_ROOM);
             return;
         }
         n_tok = len + a.T;
@@ -120,11 +129,12 @@ __device__ __forceinline__ void replay_pertoken(const ReplayArgs &a)
         n_tok = len;
     }
     const int cap = a.cap, T = a.T, H = a.H;
-    float *sk = smem;                                    // [cap][DK]
-    float *sq = sk + (size_t)cap * DK;                   // [T][DK]
-    float *sv = sq + (size_t)T * DK;                     // [cap][DV]
-    float *sa = sv + (size_t)cap * DV;                   // [cap] alpha
-    float *sb = sa + cap;                                // [cap] beta
+    const int cmax = MODE == kVerifyFold ? cap + T : cap;   // most tokens one unit replays
+    float *sk = smem;                                    // [cmax][DK]
+    float *sq = sk + (size_t)cmax * DK;                  // [T][DK]
+    float *sv = sq + (size_t)T * DK;                     // [cmax][DV]
+    float *sa = sv + (size_t)cmax * DV;                  // [cmax] alpha
+    float *sb = sa + cmax;                               // [cmax] beta
 
     const size_t unit = (size_t)slot * H + h;
     const TIn *bk = reinterpret_cast<const TIn *>(a.buf_k) + unit * cap * DK;
@@ -136,7 +146,7 @@ __device__ __forceinline__ void replay_pertoken(const ReplayArgs &a)
     stage_rows<TIn, DV>(sv, 0, len, bv, DV, nullptr, 0);
     for (int t = threadIdx.x; t < len; t += blockDim.x) { sa[t] = expf(bg[t]); sb[t] = bb[t]; }
     if (VERIFY) {
-        const bool writer = blockIdx.z == 0;             // one CTA per (b, h) stages the draft
+        const bool writer = blockIdx.z == 0 && !fold;    // one CTA per (b, h) stages the draft
         const long tk = (long)H * DK, tv = (long)H * DV;
         const TIn *dk_ = reinterpret_cast<const TIn *>(a.k) + ((size_t)b * T * H + h) * DK;
         const TIn *dq_ = reinterpret_cast<const TIn *>(a.q) + ((size_t)b * T * H + h) * DK;
@@ -161,13 +171,13 @@ __device__ __forceinline__ void replay_pertoken(const ReplayArgs &a)
 
     // ---- state row chunk into registers
     constexpr int NC = 4;                                // float4 chunks per thread
-    const int row = blockIdx.z * kRows + threadIdx.x / TPR, part = threadIdx.x % TPR;
-    const float *src = (VERIFY ? a.state_in : a.state_out) + (unit * DV + row) * DK;
+    const int row = blockIdx.z * ROWS + threadIdx.x / TPR, part = threadIdx.x % TPR;
+    const float *src = (MODE == kVerify ? a.state_in : a.state_out) + (unit * DV + row) * DK;
     float4 s[NC];
 #pragma unroll
     for (int m = 0; m < NC; ++m)                         // flush rewrites what it reads: coherent loads
-        s[m] = VERIFY ? __ldg(reinterpret_cast<const float4 *>(src) + TPR * m + part)
-                      : reinterpret_cast<const float4 *>(src)[TPR * m + part];
+        s[m] = MODE == kVerify ? __ldg(reinterpret_cast<const float4 *>(src) + TPR * m + part)
+                               : reinterpret_cast<const float4 *>(src)[TPR * m + part];
 
     float c = 1.0f;
     for (int t = 0; t < n_tok; ++t) {
@@ -194,6 +204,12 @@ __device__ __forceinline__ void replay_pertoken(const ReplayArgs &a)
             for (int m = 0; m < NC; ++m) { s[m].x *= c; s[m].y *= c; s[m].z *= c; s[m].w *= c; }
             c = 1.0f;
         }
+        if (MODE == kVerifyFold && fold && t == len - 1) {   // the flushed checkpoint
+            float4 *dst = reinterpret_cast<float4 *>(a.state_out + (unit * DV + row) * DK);
+#pragma unroll
+            for (int m = 0; m < NC; ++m)
+                dst[TPR * m + part] = make_float4(s[m].x * c, s[m].y * c, s[m].z * c, s[m].w * c);
+        }
         if (VERIFY && t >= len) {
             const float4 *qt = reinterpret_cast<const float4 *>(sq + (size_t)(t - len) * DK);
             float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -213,16 +229,46 @@ __device__ __forceinline__ void replay_pertoken(const ReplayArgs &a)
         for (int m = 0; m < NC; ++m)
             dst[TPR * m + part] = make_float4(s[m].x * c, s[m].y * c, s[m].z * c, s[m].w * c);
     }
+    if (MODE == kVerifyFold && fold) {
+        // the draft becomes buffer tokens 0 .. T-1; every buffer read was staged before
+        // the barrier above, and this CTA is the only reader of the unit's buffer
+        const int T = a.T, H = a.H, cap = a.cap;
+        constexpr int VE = InVec<TIn>::N;
+        TIn *wk = reinterpret_cast<TIn *>(a.buf_k) + unit * cap * DK;
+        TIn *wv = reinterpret_cast<TIn *>(a.buf_v) + unit * cap * DV;
+        const TIn *dk_ = reinterpret_cast<const TIn *>(a.k) + ((size_t)b * T * H + h) * DK;
+        const TIn *dv_ = reinterpret_cast<const TIn *>(a.v) + ((size_t)b * T * H + h) * DV;
+        for (int e = threadIdx.x; e < T * (DK / VE); e += blockDim.x) {
+            const int r = e / (DK / VE), cc = e % (DK / VE);
+            reinterpret_cast<uint4 *>(wk + (size_t)r * DK)[cc] =
+                __ldg(reinterpret_cast<const uint4 *>(dk_ + (size_t)r * H * DK) + cc);
+        }
+        for (int e = threadIdx.x; e < T * (DV / VE); e += blockDim.x) {
+            const int r = e / (DV / VE), cc = e % (DV / VE);
+            reinterpret_cast<uint4 *>(wv + (size_t)r * DV)[cc] =
+                __ldg(reinterpret_cast<const uint4 *>(dv_ + (size_t)r * H * DV) + cc);
+        }
+        for (int t = threadIdx.x; t < T; t += blockDim.x) {
+            const size_t gi = ((size_t)b * T + t) * H + h;
+            a.buf_g[unit * cap + t] = a.g[gi];
+            a.buf_beta[unit * cap + t] = a.beta[gi];
+        }
+    }
 }
 
 template <int DK, int DV, typename TIn>
 __global__ void __launch_bounds__(kRows * (DK / 16), 2) verify_pertoken_kernel(ReplayArgs a) {
-    replay_pertoken<DK, DV, TIn, true>(a);
+    replay_pertoken<DK, DV, TIn, kVerify>(a);
 }
 
 template <int DK, int DV, typename TIn>
 __global__ void __launch_bounds__(kRows * (DK / 16), 2) flush_pertoken_kernel(ReplayArgs a) {
-    replay_pertoken<DK, DV, TIn, false>(a);
+    replay_pertoken<DK, DV, TIn, kFlush>(a);
+}
+
+template <int DK, int DV, typename TIn>
+__global__ void __launch_bounds__(DV * (DK / 16), 1) verify_fold_pertoken_kernel(ReplayArgs a) {
+    replay_pertoken<DK, DV, TIn, kVerifyFold>(a);
 }
 
 // After the flush kernel: one thread per sequence resets the length of every
@@ -254,6 +300,24 @@ __global__ void accept_kernel(int32_t *buf_len, const int32_t *state_idx, const 
     buf_len[slot] = len + p;
 }
 
+// After a verify with fold: sequences whose buffer reached the threshold restart
+// at length 0 (their draft sits in slots 0 .. T-1), then the accepted prefix is kept.
+__global__ void accept_fold_kernel(int32_t *buf_len, const int32_t *state_idx, const int32_t *accepted,
+                                   int B, int n_slot, int T, int cap, int threshold, int32_t *status)
+{
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const int slot = state_idx ? state_idx[b] : b;
+    if (slot < 0 || slot >= n_slot) { atomicOr(status, GDN_STATUS_BAD_SLOT); return; }
+    const int p = accepted[b];
+    if (p < 0 || p > T) { atomicOr(status, GDN_STATUS_BAD_ACCEPT); return; }
+    int len = buf_len[slot];
+    if (len < 0 || len > cap) { atomicOr(status, GDN_STATUS_BAD_LEN); return; }
+    if (len >= threshold) len = 0;
+    if (len + p > cap) { atomicOr(status, GDN_STATUS_BAD_LEN); return; }
+    buf_len[slot] = len + p;
+}
+
 // ------------------------------------------------------------------ host side
 bool aligned(const void *p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
@@ -269,24 +333,29 @@ int check_dims(const gdn_replay_dims *d) {
     return GDN_OK;
 }
 
-template <int DK, int DV, typename TIn, bool VERIFY>
+template <int DK, int DV, typename TIn, int MODE>
 int launch_replay(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s) {
-    auto kern = VERIFY ? verify_pertoken_kernel<DK, DV, TIn> : flush_pertoken_kernel<DK, DV, TIn>;
-    const size_t smem = replay_smem_floats(DK, DV, d->cap, d->T) * sizeof(float);
+    auto kern = MODE == kVerify ? verify_pertoken_kernel<DK, DV, TIn>
+              : MODE == kFlush  ? flush_pertoken_kernel<DK, DV, TIn>
+                                : verify_fold_pertoken_kernel<DK, DV, TIn>;
+    const size_t smem = replay_smem_floats(DK, DV, MODE == kVerifyFold ? d->cap + d->T : d->cap, d->T) *
+                        sizeof(float);
+    if (smem > 227 * 1024) return GDN_ERR_DIMS;
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return GDN_ERR_LAUNCH;
-    kern<<<dim3(d->H, d->B, DV / kRows), kRows * (DK / 16), smem, s>>>(a);
+    const int rows = MODE == kVerifyFold ? DV : kRows;
+    kern<<<dim3(d->H, d->B, DV / rows), rows * (DK / 16), smem, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
-template <bool VERIFY>
+template <int MODE>
 int dispatch_replay(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s) {
     const bool bf = d->in_dtype == GDN_DTYPE_BF16;
 #define GDN_CASE(DK_, DV_)                                                                   \
     if (d->dk == DK_ && d->dv == DV_)                                                        \
-        return bf ? launch_replay<DK_, DV_, __nv_bfloat16, VERIFY>(d, a, s)                  \
-                  : launch_replay<DK_, DV_, float, VERIFY>(d, a, s);
+        return bf ? launch_replay<DK_, DV_, __nv_bfloat16, MODE>(d, a, s)                    \
+                  : launch_replay<DK_, DV_, float, MODE>(d, a, s);
     GDN_CASE(128, 128) GDN_CASE(128, 64) GDN_CASE(64, 128) GDN_CASE(64, 64)
 #undef GDN_CASE
     return GDN_ERR_DIMS;
@@ -317,9 +386,9 @@ int gdn_replay_verify(const gdn_replay_dims *d, const float *state, const int32_
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = out; a.status = status;
     a.B = d->B; a.H = d->H; a.T = d->T; a.cap = d->cap; a.threshold = d->threshold;
     a.n_slot = d->n_slot; a.scale = d->scale;
-    const int tc = gdn::tc_verify(d, a, stream);
+    const int tc = gdn::tc_verify(d, a, stream, false);
     if (tc <= 0) return tc;
-    return dispatch_replay<true>(d, a, stream);
+    return dispatch_replay<kVerify>(d, a, stream);
 }
 
 int gdn_replay_accept(const gdn_replay_dims *d, int32_t *buf_len, const int32_t *state_idx,
@@ -352,10 +421,49 @@ int gdn_replay_flush(const gdn_replay_dims *d, float *state, const int32_t *stat
     a.B = d->B; a.H = d->H; a.T = d->T; a.cap = d->cap; a.threshold = d->threshold;
     a.force = force ? 1 : 0; a.n_slot = d->n_slot; a.scale = d->scale;
     int r = gdn::tc_flush(d, a, stream);
-    if (r > 0) r = dispatch_replay<false>(d, a, stream);
+    if (r > 0) r = dispatch_replay<kFlush>(d, a, stream);
     if (r) return r;
     flush_lengths_kernel<<<(d->B + 127) / 128, 128, 0, stream>>>(buf_len, state_idx, d->B, d->n_slot,
                                                                   d->cap, d->threshold, a.force, status);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+}
+
+int gdn_replay_verify_fold(const gdn_replay_dims *d, float *state, const int32_t *state_idx,
+                           void *buf_k, void *buf_v, float *buf_g, float *buf_beta,
+                           const int32_t *buf_len, const void *q, const void *k, const void *v,
+                           const float *g, const float *beta, float *out, int32_t *status,
+                           cudaStream_t stream)
+{
+    const int rc = check_dims(d);
+    if (rc) return rc;
+    if (d->B == 0) return GDN_OK;
+    if (!state || !buf_k || !buf_v || !buf_g || !buf_beta || !buf_len || !q || !k || !v || !g ||
+        !beta || !out || !status)
+        return GDN_ERR_NULL;
+    if (!aligned(state, 16) || !aligned(buf_k, 16) || !aligned(buf_v, 16) || !aligned(q, 16) ||
+        !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 4))
+        return GDN_ERR_DIMS;
+    if (d->threshold + d->T - 1 > d->cap) return GDN_ERR_DIMS;   // room for the draft when not folding
+    ReplayArgs a{};
+    a.state_in = state; a.state_out = state; a.state_idx = state_idx;
+    a.buf_k = buf_k; a.buf_v = buf_v; a.buf_g = buf_g; a.buf_beta = buf_beta; a.buf_len = buf_len;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = out; a.status = status;
+    a.B = d->B; a.H = d->H; a.T = d->T; a.cap = d->cap; a.threshold = d->threshold;
+    a.n_slot = d->n_slot; a.scale = d->scale;
+    const int tc = gdn::tc_verify(d, a, stream, true);
+    if (tc <= 0) return tc;
+    return dispatch_replay<kVerifyFold>(d, a, stream);
+}
+
+int gdn_replay_accept_fold(const gdn_replay_dims *d, int32_t *buf_len, const int32_t *state_idx,
+                           const int32_t *accepted, int32_t *status, cudaStream_t stream)
+{
+    const int rc = check_dims(d);
+    if (rc) return rc;
+    if (d->B == 0) return GDN_OK;
+    if (!buf_len || !accepted || !status) return GDN_ERR_NULL;
+    accept_fold_kernel<<<(d->B + 127) / 128, 128, 0, stream>>>(buf_len, state_idx, accepted, d->B, d->n_slot,
+                                                                d->T, d->cap, d->threshold, status);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
 

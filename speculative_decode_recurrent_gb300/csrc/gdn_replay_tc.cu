@@ -154,20 +154,43 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 &raw, float *f) {
 
 __host__ __device__ inline int round16(int x) { return (x + 15) & ~15; }
 
-// Shared-memory plan of the verify kernel (bytes from the 1024-aligned base):
-//   [0, 64K)           S0 tile (fp32, 4 sub-tiles of 128 rows x 128 B); after the
-//                      MMAs: rhs_t = beta_t (v_t - gamma_t P_t) and P_q columns
-//   [64K, 64K + SB)    [K;Q] fp32 tile, 4 sub-tiles of NP rows x 128 B, plus
-//                      slack so an M=128 operand may read past row NP;
-//                      after the MMAs: the coefficient matrices (row stride CP+4)
-//   then: 2 mbarriers, TMEM slot, flag, and G (hi, lo), beta, gamma per token, each
-//   array padded to a multiple of 16 tokens so it can be read as float4.
-__host__ __device__ inline int verify_sb_bytes(int cap, int T) { return (3 * round16(cap + T) + 128) * 128; }
-__host__ __device__ inline int verify_smem_bytes(int cap, int T) {
-    return 1024 + 65536 + verify_sb_bytes(cap, T) + 64 + 16 * round16(cap + T);
+// Three bf16 terms whose sum is x exactly (for normal-range x): each rounding
+// to bf16 keeps the next 8-9 significant bits of what is left.
+__device__ __forceinline__ void split3(float x, __nv_bfloat16 &h, __nv_bfloat16 &m, __nv_bfloat16 &l) {
+    h = __float2bfloat16_rn(x);
+    const float r1 = x - __bfloat162float(h);
+    m = __float2bfloat16_rn(r1);
+    l = __float2bfloat16_rn(r1 - __bfloat162float(m));
+}
+__device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
+    return static_cast<uint32_t>(__bfloat16_as_ushort(a)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
 }
 
-template <int CMAX>
+// Shared-memory plan of the verify kernel (bytes from the 1024-aligned base):
+//   [0, 64K)          S0 tile (fp32, 4 sub-tiles of 128 rows x 128 B, TMA).  After the
+//                     MMAs, in a folding unit: U~ as three bf16 tiles [0, 48K) and K^T
+//                     (bf16) [48K, 64K) for the fold MMA, then the new state for the
+//                     TMA store.
+//   [64K, 64K + SB)   [K;Q] fp32 tile, 4 sub-tiles of NP rows x 128 B, plus slack so an
+//                     M=128 operand may read past row NP.  After the MMAs: coefficient
+//                     matrices (row stride CP+4) followed by the S0 q columns.
+//   then: 4 mbarriers, TMEM slot, flags, and G (hi, lo), beta, gamma per token, each
+//   array padded to a multiple of 16 tokens so it can be read as float4.
+// cmax = most tokens one unit replays: cap (verify), cap + T (verify with fold, where a
+// full buffer is replayed together with the draft).  The dynamic shared memory base is
+// the start of the CTA's shared window (no static shared variables), so it is 1024-byte
+// aligned; the kernel checks this and, if it ever fails, reports it in the status word
+// and skips the unit.
+__host__ __device__ inline int verify_sb_bytes(int cmax, int T) { return (3 * round16(cmax + T) + 128) * 128; }
+__host__ __device__ inline int verify_smem_bytes(int cmax, int T) {
+    return 65536 + verify_sb_bytes(cmax, T) + 64 + 16 * round16(cmax);
+}
+
+// FOLD = false: gdn_replay_verify.  FOLD = true: gdn_replay_verify_fold -- a unit whose
+// buffer has reached the threshold also writes the checkpoint after its buffered
+// tokens (the flush, done here instead of in a separate pass over the state) and
+// stages the draft at buffer slot 0.
+template <int CMAX, bool FOLD>
 __global__ void __launch_bounds__(kThreads, 2)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
 {
@@ -179,35 +202,43 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     }
     const int len = a.buf_len[slot];
     const int T = a.T, H = a.H, cap = a.cap;
-    if (len < 0 || len + T > cap) {
-        if (tid == 0 && h == 0) atomicOr(a.status, GDN_STATUS_NO_ROOM);
+    const bool fold = FOLD && len >= a.threshold && len <= cap;
+    if (len < 0 || (!fold && len + T > cap)) {
+        if (tid == 0 && h == 0) atomicOr(a.status, len < 0 || len > cap ? GDN_STATUS_BAD_LEN : GDN_STATUS_NO_ROOM);
         return;
     }
     const int C = len + T;                   // replayed tokens: buffer, then draft
     const int NP = round16(C + T);           // rows of the [K;Q] operand
     const int CP = round16(C);               // key columns of the K.K / Q.K product
     const int LDA = CP + 4;
+    const int row0 = fold ? 0 : len;         // buffer slot of draft token 0
+    const int cmax = FOLD ? cap + T : cap;
 
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (saddr(smem_raw) & 1023u) {           // the swizzled tiles need a 1024-byte aligned base
+        if (tid == 0) atomicOr(a.status, kStatusTimeout);
+        return;
+    }
+    uint8_t *base = smem_raw;
     uint8_t *sA = base;
     uint8_t *sB = base + 65536;
-    uint8_t *sm = sB + verify_sb_bytes(cap, T);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm);            // [0] TMA, [1] MMA
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + 16);
-    int *flag = reinterpret_cast<int *>(sm + 20);
-    const int GS = round16(cap + T);                              // per-token array stride (16-B rows)
+    uint8_t *sm = sB + verify_sb_bytes(cmax, T);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm);            // TMA, K.K MMA, P MMA, fold MMA
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + 32);
+    int *flag = reinterpret_cast<int *>(sm + 36);
+    const int GS = round16(cmax);                                 // per-token array stride (16-B rows)
     float *sGh = reinterpret_cast<float *>(sm + 64);
     float *sGl = sGh + GS;
     float *sBeta = sGl + GS;
     float *sGam = sBeta + GS;
     float *sMat = reinterpret_cast<float *>(sB);                  // reused after the MMAs
-    float *sR = reinterpret_cast<float *>(sA);                    // reused after the MMAs: [C][128]
-    float *sPQ = sR + static_cast<size_t>(C) * 128;               //                        [T][128]
+    float *sPQ = sMat + static_cast<size_t>(C + T) * LDA;         // [T][128]
+    uint8_t *sU = sA;                                             // fold: 3 x 16 KB
+    uint8_t *sKt = sA + 49152;                                    // fold: 16 KB
 
     if (tid == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
         *flag = 0;
         fence_mbar_init();
     }
@@ -218,11 +249,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     const uint32_t tmem = *tmem_slot;
 
     const size_t unit = static_cast<size_t>(slot) * H + h;
+    const int ytile = static_cast<int>(unit) * 128;
     if (tid == 0) {                                               // checkpoint tile by TMA
         mbar_expect_tx(&bar[0], 65536);
-        const int y = static_cast<int>(unit) * 128;
 #pragma unroll
-        for (int kb = 0; kb < 4; ++kb) tma_load_2d(sA + kb * 16384, &tm_state, kb * 32, y, &bar[0]);
+        for (int kb = 0; kb < 4; ++kb) tma_load_2d(sA + kb * 16384, &tm_state, kb * 32, ytile, &bar[0]);
     }
 
     // ---- every global load of this unit, issued back to back (one memory latency)
@@ -233,8 +264,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     const __nv_bfloat16 *dk = reinterpret_cast<const __nv_bfloat16 *>(a.k) + drow0;
     const __nv_bfloat16 *dq = reinterpret_cast<const __nv_bfloat16 *>(a.q) + drow0;
     const __nv_bfloat16 *dv = reinterpret_cast<const __nv_bfloat16 *>(a.v) + drow0;
-    __nv_bfloat16 *wk = reinterpret_cast<__nv_bfloat16 *>(a.buf_k) + (unit * cap + len) * 128;
-    __nv_bfloat16 *wv = reinterpret_cast<__nv_bfloat16 *>(a.buf_v) + (unit * cap + len) * 128;
+    __nv_bfloat16 *wk = reinterpret_cast<__nv_bfloat16 *>(a.buf_k) + (unit * cap + row0) * 128;
+    __nv_bfloat16 *wv = reinterpret_cast<__nv_bfloat16 *>(a.buf_v) + (unit * cap + row0) * 128;
     constexpr int NV = (CMAX + 16) * 16 / kThreads;               // 16-byte vectors of [K;Q] per thread
     uint4 raw[NV];
 #pragma unroll
@@ -246,12 +277,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
                                                : dq + static_cast<size_t>(r - C) * dstride;
             raw[i] = __ldg(reinterpret_cast<const uint4 *>(src) + c);
         }
-    }
-    uint4 rawv[2];                                                // draft values, staged to the buffer
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
-        if (r < T) rawv[i] = __ldg(reinterpret_cast<const uint4 *>(dv + static_cast<size_t>(r) * dstride) + c);
     }
     // value channel `tid` of every token: unconditional loads from clamped addresses so
     // that all of them are in flight together; widened to fp32 only when first used
@@ -280,12 +305,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
             }
         }
     }
-    // ---- widen [K;Q] into the swizzled fp32 tile; draft k, v, g, beta -> buffer
+    // ---- widen [K;Q] into the swizzled fp32 tile; draft keys into the buffer (no fold)
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
         if (r < C + T) {
-            if (r >= len && r < C) reinterpret_cast<uint4 *>(wk + static_cast<size_t>(r - len) * 128)[c] = raw[i];
+            if (!fold && r >= len && r < C) reinterpret_cast<uint4 *>(wk + static_cast<size_t>(r - len) * 128)[c] = raw[i];
             float f[8];
             bf16x8_to_f32(raw[i], f);
             uint8_t *tile = sB + (c >> 2) * NP * 128;
@@ -293,11 +318,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
             *reinterpret_cast<float4 *>(tile + sw128(r, ch)) = make_float4(f[0], f[1], f[2], f[3]);
             *reinterpret_cast<float4 *>(tile + sw128(r, ch + 1)) = make_float4(f[4], f[5], f[6], f[7]);
         }
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
-        if (r < T) reinterpret_cast<uint4 *>(wv + static_cast<size_t>(r) * 128)[c] = rawv[i];
     }
     if (warp == 0) {
         // running log-decay G_t = sum_{s<=t} g_s as a compensated pair (hi + lo): a
@@ -333,11 +353,18 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
                 sGl[t] = lo[i];
                 sGam[t] = __expf(hi[i] + lo[i]);
                 sBeta[t] = bq[i];
-                if (t >= len) {
+                if (!fold && t >= len) {
                     a.buf_g[unit * cap + t] = gq[i];
                     a.buf_beta[unit * cap + t] = bq[i];
                 }
             }
+        }
+    }
+    if (!fold) {
+        for (int e = tid; e < T * 16; e += kThreads) {            // draft values into the buffer
+            const int r = e >> 4, c = e & 15;
+            reinterpret_cast<uint4 *>(wv + static_cast<size_t>(r) * 128)[c] =
+                __ldg(reinterpret_cast<const uint4 *>(dv + static_cast<size_t>(r) * dstride) + c);
         }
     }
     fence_proxy_async();                      // generic writes of the [K;Q] tile -> async proxy
@@ -348,18 +375,18 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
             const uint32_t idP = idesc_mn(2, 128, NP), idK = idesc_mn(2, 128, CP);
             const uint32_t a0 = saddr(sA), b0 = saddr(sB);
 #pragma unroll
-            for (int ks = 0; ks < 16; ++ks) {                      // K = 128 in steps of 8 (32 bytes)
+            for (int ks = 0; ks < 16; ++ks) {                      // [K;Q] K^T first (coefficients)
+                const uint64_t d = desc_sw128(b0 + (ks >> 2) * NP * 128 + (ks & 3) * 32);
+                mma_tf32(tmem + NP, d, d, idK, ks > 0);
+            }
+            mma_commit(&bar[1]);
+#pragma unroll
+            for (int ks = 0; ks < 16; ++ks) {                      // P = S0 [K;Q]^T, K = 128 in steps of 8
                 const uint32_t off = (ks & 3) * 32;
                 mma_tf32(tmem, desc_sw128(a0 + (ks >> 2) * 16384 + off),
                          desc_sw128(b0 + (ks >> 2) * NP * 128 + off), idP, ks > 0);
             }
-#pragma unroll
-            for (int ks = 0; ks < 16; ++ks) {
-                const uint32_t off = (ks & 3) * 32;
-                const uint64_t d = desc_sw128(b0 + (ks >> 2) * NP * 128 + off);
-                mma_tf32(tmem + NP, d, d, idK, ks > 0);
-            }
-            mma_commit(&bar[1]);
+            mma_commit(&bar[2]);
         } else {
             *flag = 1;
         }
@@ -371,7 +398,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
         // give up on this unit: wait (bounded) for in-flight copies / MMAs, report, free TMEM
         if (tid == 0) {
             mbar_wait(&bar[0], 0);
-            if (*flag == 0) mbar_wait(&bar[1], 0);
+            if (*flag == 0) {
+                mbar_wait(&bar[1], 0);
+                mbar_wait(&bar[2], 0);
+            }
             atomicOr(a.status, kStatusTimeout);
         }
         tc_fence_before();
@@ -382,16 +412,23 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     tc_fence_after();
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
 
-    // ---- coefficient rows from K.K / Q.K (TMEM lane = token)
-    for (int c0 = 0; c0 < CP; c0 += 16) {
-        float kq[16];
-        tmem_ld16(lane_base + NP + c0, kq);
-        if (tid < C + T) {
-            const bool is_q = tid >= C;
-            const int p = is_q ? len + (tid - C) : tid;          // position of this row's token
-            const float gh = sGh[p], gl = sGl[p];
-            const float scl = is_q ? 1.f : sBeta[tid];
-            const int lim = is_q ? min(p + 1, C) : tid;           // columns s < lim are used
+    // ---- coefficient rows from K.K / Q.K (TMEM lane = token), kept in registers until
+    //      the P MMA has finished reading the [K;Q] tile they will be written over:
+    //      A[t][s] = beta_t e^{G_t-G_s} (k_t.k_s) for s < t, M[t'][s] = e^{G_p-G_s} (q_t'.k_s)
+    //      for s <= p = len + t'
+    float m[CMAX / 16][16];
+    {
+        const bool is_q = tid >= C;
+        const int p = tid >= C + T ? C - 1 : is_q ? len + (tid - C) : tid;   // position of this row's token
+        const float gh = sGh[p], gl = sGl[p];
+        const float scl = is_q ? 1.f : sBeta[p];
+        const int lim = tid >= C + T ? 0 : is_q ? min(p + 1, C) : tid;   // columns s < lim are used
+#pragma unroll
+        for (int cb = 0; cb < CMAX / 16; ++cb) {
+            const int c0 = cb * 16;
+            if (c0 >= CP) break;
+            float kq[16];
+            tmem_ld16(lane_base + NP + c0, kq);
             float gs[16], ls[16];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -400,50 +437,82 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
                 gs[4 * j] = x.x; gs[4 * j + 1] = x.y; gs[4 * j + 2] = x.z; gs[4 * j + 3] = x.w;
                 ls[4 * j] = y.x; ls[4 * j + 1] = y.y; ls[4 * j + 2] = y.z; ls[4 * j + 3] = y.w;
             }
-            float m[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const float e = __expf((gh - gs[j]) + (gl - ls[j]));
-                m[j] = (c0 + j < lim) ? scl * e * kq[j] : 0.f;
+                m[cb][j] = (c0 + j < lim) ? scl * e * kq[j] : 0.f;
             }
-            float4 *dst = reinterpret_cast<float4 *>(sMat + static_cast<size_t>(tid) * LDA + c0);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = make_float4(m[4 * j], m[4 * j + 1], m[4 * j + 2], m[4 * j + 3]);
         }
     }
-    // ---- right-hand sides rhs_t = beta_t (v_t - gamma_t (S0 k_t)) and the S0 q columns
+    // ---- the P MMA has landed: S0 q columns, fold K^T, then the coefficient rows
+    ok = mbar_wait(&bar[2], 0);
+    if (__syncthreads_or(!ok)) {
+        if (tid == 0) {
+            mbar_wait(&bar[2], 0);
+            atomicOr(a.status, kStatusTimeout);
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+        return;
+    }
+    tc_fence_after();
+    float pq[2][16];
 #pragma unroll
-    for (int c0 = 0; c0 < CMAX; c0 += 16) {                       // key columns [0, C)
-        if (c0 >= C) break;
-        float pc[16];
-        tmem_ld16(lane_base + c0, pc);
+    for (int i = 0; i < 2; ++i) {                                 // columns [C & ~15, +32) hold S0 q
+        const int c0 = (C & ~15) + 16 * i;
+        if (c0 < C + T) tmem_ld16(lane_base + c0, pq[i]);
+    }
+    if (fold) {                                                   // K^T (bf16) from the fp32 key tile
+        const __nv_bfloat16 zero = __float2bfloat16_rn(0.f);
+        const uint8_t *colbase = sB + (tid >> 5) * NP * 128 + (tid & 3) * 4;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int t = c0 + j;
-            if (t < C)
-                sR[static_cast<size_t>(t) * 128 + tid] =
-                    sBeta[t] * (__bfloat162float(__ushort_as_bfloat16(vraw[t])) - sGam[t] * pc[j]);
+        for (int c8 = 0; c8 < CMAX / 8; ++c8) {
+            __nv_bfloat16 kk[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int s = c8 * 8 + j;
+                kk[j] = s < len ? __float2bfloat16_rn(*reinterpret_cast<const float *>(
+                                      colbase + sw128(s, (tid & 31) >> 2)))
+                                : zero;
+            }
+            *reinterpret_cast<uint4 *>(sKt + sw128(tid, c8)) =
+                make_uint4(pack2(kk[0], kk[1]), pack2(kk[2], kk[3]), pack2(kk[4], kk[5]), pack2(kk[6], kk[7]));
         }
     }
-    for (int c0 = C & ~15; c0 < C + T; c0 += 16) {                // query columns [C, C+T)
-        float pc[16];
-        tmem_ld16(lane_base + c0, pc);
+    __syncthreads();                                              // [K;Q] tile no longer read
+    if (tid < C + T) {
+#pragma unroll
+        for (int cb = 0; cb < CMAX / 16; ++cb) {
+            if (cb * 16 >= CP) break;
+            float4 *dst = reinterpret_cast<float4 *>(sMat + static_cast<size_t>(tid) * LDA + cb * 16);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                dst[j] = make_float4(m[cb][4 * j], m[cb][4 * j + 1], m[cb][4 * j + 2], m[cb][4 * j + 3]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-            const int t = c0 + j;
-            if (t >= C && t < C + T) sPQ[static_cast<size_t>(t - C) * 128 + tid] = pc[j];
+            const int t = (C & ~15) + 16 * i + j;
+            if (t >= C && t < C + T) sPQ[static_cast<size_t>(t - C) * 128 + tid] = pq[i][j];
         }
     }
     __syncthreads();
 
-    // ---- forward substitution, one state row per thread.  Coefficient rows hold zeros
-    // at s >= t and u[s] is zero until assigned, so whole 4-wide groups need no guards.
+    // ---- forward substitution, one state row per thread:
+    //   u_t = beta_t (v_t - gamma_t (S0 k_t)) - sum_{s<t} A[t][s] u_s
+    // Coefficient rows hold zeros at s >= t and u[s] is zero until assigned, so whole
+    // 4-wide groups need no guards.
     float u[CMAX];
+    float pc[16];
 #pragma unroll
     for (int t = 0; t < CMAX; ++t) u[t] = 0.f;
 #pragma unroll
     for (int t = 0; t < CMAX; ++t) {
         if (t >= C) break;
+        if ((t & 15) == 0) tmem_ld16(lane_base + t, pc);
         const float *Ar = sMat + static_cast<size_t>(t) * LDA;
         float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
 #pragma unroll
@@ -454,17 +523,54 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
             c2 = fmaf(a4.z, u[s + 2], c2);
             c3 = fmaf(a4.w, u[s + 3], c3);
         }
-        u[t] = sR[static_cast<size_t>(t) * 128 + tid] - ((c0 + c1) + (c2 + c3));
+        const float vt = __bfloat162float(__ushort_as_bfloat16(vraw[t]));
+        u[t] = sBeta[t] * (vt - sGam[t] * pc[t & 15]) - ((c0 + c1) + (c2 + c3));
+    }
+    // ---- fold: U~_s = e^{G_{len-1} - G_s} u_s (s < len) as three bf16 tiles, then
+    //      D = U~^T K on the tensor cores while the outputs below run on the ALUs
+    if (fold) {
+        const float gh = sGh[len - 1], gl = sGl[len - 1];
+#pragma unroll
+        for (int c8 = 0; c8 < CMAX / 8; ++c8) {
+            __nv_bfloat16 hh[8], mm[8], ll[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int s = c8 * 8 + j;
+                const float w = s < len ? __expf((gh - sGh[s]) + (gl - sGl[s])) * u[s] : 0.f;
+                split3(w, hh[j], mm[j], ll[j]);
+            }
+            const uint32_t off = sw128(tid, c8);
+            *reinterpret_cast<uint4 *>(sU + off) =
+                make_uint4(pack2(hh[0], hh[1]), pack2(hh[2], hh[3]), pack2(hh[4], hh[5]), pack2(hh[6], hh[7]));
+            *reinterpret_cast<uint4 *>(sU + 16384 + off) =
+                make_uint4(pack2(mm[0], mm[1]), pack2(mm[2], mm[3]), pack2(mm[4], mm[5]), pack2(mm[6], mm[7]));
+            *reinterpret_cast<uint4 *>(sU + 32768 + off) =
+                make_uint4(pack2(ll[0], ll[1]), pack2(ll[2], ll[3]), pack2(ll[4], ll[5]), pack2(ll[6], ll[7]));
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t idF = idesc_mn(1, 128, 128);
+            const uint32_t u0 = saddr(sU), kt0 = saddr(sKt);
+            const int ksteps = round16(len) / 16;
+            for (int sp = 0; sp < 3; ++sp)
+                for (int ks = 0; ks < ksteps; ++ks)
+                    mma_bf16(tmem, desc_sw128(u0 + sp * 16384 + ks * 32), desc_sw128(kt0 + ks * 32), idF,
+                             (sp | ks) != 0);
+            mma_commit(&bar[3]);
+        }
     }
     // ---- draft outputs o_t = scale (gamma_p S0 q_t + sum_{s<=p} e^{G_p-G_s} (q_t.k_s) u_s);
-    // the coefficient rows are zero past p and past C, so every row sums over [0, CP)
+    // the coefficient rows are zero past p, so each sum stops at the 16-block holding p
     for (int t2 = 0; t2 < T; ++t2) {
         const int p = len + t2;
         const float *Mr = sMat + static_cast<size_t>(C + t2) * LDA;
         float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
 #pragma unroll
         for (int s = 0; s < CMAX; s += 4) {
-            if ((s & 15) == 0 && s >= CP) break;
+            if ((s & 15) == 0 && s > p) break;
             const float4 m4 = *reinterpret_cast<const float4 *>(Mr + s);
             c0 = fmaf(m4.x, u[s], c0);
             c1 = fmaf(m4.y, u[s + 1], c1);
@@ -474,22 +580,67 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
         const float o = sGam[p] * sPQ[static_cast<size_t>(t2) * 128 + tid] + ((c0 + c1) + (c2 + c3));
         a.out[((static_cast<size_t>(b) * T + t2) * H + h) * 128 + tid] = a.scale * o;
     }
+    if (fold) {
+        // ---- new checkpoint S_len = gamma_{len-1} S0 + D, written over the S0 tile and
+        //      stored by TMA; S0 row `tid` is read again from global memory (L2)
+        const float4 *s0 = reinterpret_cast<const float4 *>(a.state_in + (unit * 128 + tid) * 128);
+        float4 x[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) x[q] = s0[q];
+        ok = mbar_wait(&bar[3], 0);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) {
+                mbar_wait(&bar[3], 0);
+                atomicOr(a.status, kStatusTimeout);
+            }
+            tc_fence_before();
+            __syncthreads();
+            if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+            return;
+        }
+        tc_fence_after();
+        const float gL = sGam[len - 1];
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 16) {
+            float d[16];
+            tmem_ld16(lane_base + c0, d);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int col = c0 + 4 * q;
+                float4 y = x[col >> 2];
+                y.x = fmaf(gL, y.x, d[4 * q]);
+                y.y = fmaf(gL, y.y, d[4 * q + 1]);
+                y.z = fmaf(gL, y.z, d[4 * q + 2]);
+                y.w = fmaf(gL, y.w, d[4 * q + 3]);
+                *reinterpret_cast<float4 *>(sA + (col >> 5) * 16384 + sw128(tid, (col & 31) >> 2)) = y;
+            }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+#pragma unroll
+            for (int kb = 0; kb < 4; ++kb) tma_store_2d(&tm_state, kb * 32, ytile, sA + kb * 16384);
+            tma_store_commit_and_wait();
+        }
+        // ---- the draft becomes buffer tokens 0 .. T-1 (every read of the old buffer is done)
+        for (int e = tid; e < T * 16; e += kThreads) {
+            const int r = e >> 4, c = e & 15;
+            reinterpret_cast<uint4 *>(wk + static_cast<size_t>(r) * 128)[c] =
+                __ldg(reinterpret_cast<const uint4 *>(dk + static_cast<size_t>(r) * dstride) + c);
+            reinterpret_cast<uint4 *>(wv + static_cast<size_t>(r) * 128)[c] =
+                __ldg(reinterpret_cast<const uint4 *>(dv + static_cast<size_t>(r) * dstride) + c);
+        }
+        for (int t = tid; t < T; t += kThreads) {
+            const size_t gi = (static_cast<size_t>(b) * T + t) * H + h;
+            a.buf_g[unit * cap + t] = a.g[gi];
+            a.buf_beta[unit * cap + t] = a.beta[gi];
+        }
+    }
 
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
-}
-
-// Three bf16 terms whose sum is x exactly (for normal-range x): each rounding
-// to bf16 keeps the next 8-9 significant bits of what is left.
-__device__ __forceinline__ void split3(float x, __nv_bfloat16 &h, __nv_bfloat16 &m, __nv_bfloat16 &l) {
-    h = __float2bfloat16_rn(x);
-    const float r1 = x - __bfloat162float(h);
-    m = __float2bfloat16_rn(r1);
-    l = __float2bfloat16_rn(r1 - __bfloat162float(m));
-}
-__device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
-    return static_cast<uint32_t>(__bfloat16_as_ushort(a)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
 }
 
 // Shared-memory plan of the flush kernel (bytes from the 1024-aligned base):
@@ -856,10 +1007,10 @@ bool state_map(CUtensorMap *m, const float *state, int rows) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int CMAX>
+template <int CMAX, bool FOLD>
 int launch_verify(const gdn_replay_dims *d, const ReplayArgs &a, const CUtensorMap &m, cudaStream_t s) {
-    const int smem = verify_smem_bytes(d->cap, d->T);
-    auto kern = verify_tc_kernel<CMAX>;
+    const int smem = verify_smem_bytes(FOLD ? d->cap + d->T : d->cap, d->T);
+    auto kern = verify_tc_kernel<CMAX, FOLD>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return GDN_ERR_LAUNCH;
     kern<<<dim3(d->H, d->B), kThreads, smem, s>>>(m, a);
@@ -868,13 +1019,15 @@ int launch_verify(const gdn_replay_dims *d, const ReplayArgs &a, const CUtensorM
 
 }  // namespace
 
-int tc_verify(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s) {
+int tc_verify(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s, bool fold) {
     if (d->dk != 128 || d->dv != 128 || d->in_dtype != GDN_DTYPE_BF16) return 1;
-    if (d->cap > 64 || d->T > 16) return 1;                       // C <= 64 tokens, T <= 16 queries
-    if (verify_smem_bytes(d->cap, d->T) > 227 * 1024) return 1;
+    const int cmax = fold ? d->cap + d->T : d->cap;               // tokens one unit may replay
+    if (cmax > 64 || d->T > 16) return 1;                         // register arrays hold 64 tokens
+    if (verify_smem_bytes(cmax, d->T) > 227 * 1024) return 1;
     CUtensorMap m;
     if (!state_map(&m, a.state_in, d->n_slot * d->H * 128)) return 1;
-    return d->cap <= 48 ? launch_verify<48>(d, a, m, s) : launch_verify<64>(d, a, m, s);
+    if (fold) return cmax <= 48 ? launch_verify<48, true>(d, a, m, s) : launch_verify<64, true>(d, a, m, s);
+    return cmax <= 48 ? launch_verify<48, false>(d, a, m, s) : launch_verify<64, false>(d, a, m, s);
 }
 
 int tc_flush(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s) {

@@ -32,7 +32,9 @@ constexpr int32_t kStatusTimeout = GDN_STATUS_TIMEOUT;
 // Tensor-core path (gdn_replay_tc.cu).  Each returns GDN_OK when it launched,
 // GDN_ERR_LAUNCH on a launch failure, and 1 when the shape is not one it
 // handles (the caller then uses the per-token kernels).
-int tc_verify(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s);
+// fold = true: units whose buffer reached the threshold also write the checkpoint
+// after their buffered tokens and stage the draft at buffer slot 0.
+int tc_verify(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s, bool fold);
 int tc_flush(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s);
 
 }  // namespace gdn

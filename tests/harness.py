@@ -85,6 +85,24 @@ class Pair:
             self.compare(out, o_ref, step)
         return out, o_ref, acc
 
+    def fused_step(self, step, check=True, accepted=None):
+        """One verify_fold -> accept_fold on the GPU against the oracle's
+        flush (threshold) -> verify -> accept, which it must equal."""
+        wl = self.wl
+        blk = self.block(step)
+        acc = blk["accepted"] if accepted is None else torch.as_tensor(accepted, dtype=torch.int32)
+        dev = {n: blk[n].to(self.device) for n in ("q", "k", "v", "g", "beta")}
+        out = torch.empty(self.B, wl.T, wl.H, wl.dv, dtype=torch.float32, device=self.device)
+        self.gpu.verify_fold(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], out)
+        self.gpu.accept_fold(acc.to(self.device))
+        self.orc.flush(force=False)
+        o_ref = self.orc.verify(blk)
+        self.orc.accept(acc.numpy())
+        torch.cuda.synchronize()
+        if check:
+            self.compare(out, o_ref, step)
+        return out, o_ref, acc
+
     def compare(self, out, o_ref, step):
         t = self.gpu.t
         tag = f"layer{self.layer}/step{step}"

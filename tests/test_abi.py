@@ -64,6 +64,18 @@ def test_bad_dims_rejected_before_launch(kw, code):
     assert so.gdn_replay_flush(ctypes.byref(d), *([FAKE] * 7), 0, FAKE, None) == code
 
 
+def test_fold_entry_points_validate():
+    so = lib.load()
+    d = good_dims(threshold=6)                 # threshold - 1 + T = 9 > cap = 8
+    assert so.gdn_replay_verify_fold(ctypes.byref(d), *([FAKE] * 14), None) == -2
+    d = good_dims()
+    assert so.gdn_replay_verify_fold(None, *([FAKE] * 14), None) == -1
+    assert so.gdn_replay_accept_fold(ctypes.byref(d), None, None, FAKE, FAKE, None) == -1
+    e = good_dims(B=0, n_slot=0)
+    assert so.gdn_replay_verify_fold(ctypes.byref(e), *([None] * 14), None) == 0
+    assert so.gdn_replay_accept_fold(ctypes.byref(e), None, None, None, None, None) == 0
+
+
 def test_null_pointers_rejected():
     so = lib.load()
     d = good_dims()

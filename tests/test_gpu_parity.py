@@ -255,3 +255,37 @@ def test_bad_slot_reported_not_dereferenced():
     pr.gpu.flush(force=True)
     torch.cuda.synchronize()
     assert int(pr.gpu.status.item()) == 8
+
+
+# --------------------------------------------- lazy flush: verify_fold + accept_fold
+@pytest.mark.parametrize("name,steps", [("b8", 16), ("edge", 12), ("tiny", 1), ("large", 3)])
+def test_fused_step_matches_flush_verify_accept(name, steps):
+    """verify_fold -> accept_fold equals flush(threshold) -> verify -> accept of the
+    oracle at every step (outputs, folded state, lengths, buffer bytes)."""
+    wl = WL[name]
+    if name == "large":
+        pr = Pair(wl, B=16)
+    else:
+        pr = Pair(wl)
+    for s in range(steps):
+        pr.fused_step(s)
+
+
+@pytest.mark.parametrize("layer", [0, 23])
+def test_fused_decode24(layer):
+    pr = Pair(WL["decode24"], layer=layer)
+    for s in range(8):
+        pr.fused_step(s)
+
+
+def test_fused_then_three_call_interleave():
+    """Both step forms keep the same buffer/length convention, so they can alternate."""
+    pr = Pair(WL["b8"])
+    for s in range(10):
+        if s % 2:
+            pr.fused_step(s)
+        else:
+            # the three-call step needs len < threshold before verify: flush first
+            pr.gpu.flush(force=False)
+            pr.orc.flush(force=False)
+            pr.step(s)
