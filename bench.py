@@ -369,7 +369,7 @@ def run_ours(args, rank, world, mode="fused"):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": args.e2e_steps}
 
-    launches_per_step = (2 if fused else 4) * L
+    launches_per_step = (3 if fused else 4) * L    # fused: fold launch + the rest + accept_fold
     del graphs, layers, pools
     torch.cuda.synchronize()
     torch.cuda.empty_cache()

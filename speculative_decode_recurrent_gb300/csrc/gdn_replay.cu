@@ -32,6 +32,9 @@
 namespace {
 
 using gdn::ReplayArgs;
+using gdn::launch_pdl;
+using gdn::pdl_release;
+using gdn::pdl_wait;
 
 constexpr int kRows = 64;               // state rows per CTA
 constexpr float kRenorm = 5.421011e-20f;  // 2^-64
@@ -108,6 +111,8 @@ __device__ __forceinline__ void replay_pertoken(const ReplayArgs &a)
     constexpr int TPR = DK / 16;                         // threads per state row
     extern __shared__ __align__(16) float smem[];
     const int h = blockIdx.x, b = blockIdx.y;
+    pdl_wait();
+    pdl_release();
     const int slot = a.state_idx ? a.state_idx[b] : b;
     if (slot < 0 || slot >= a.n_slot) {
         if (threadIdx.x == 0 && h == 0 && blockIdx.z == 0) atomicOr(a.status, GDN_STATUS_BAD_SLOT);
@@ -277,6 +282,8 @@ __global__ void __launch_bounds__(DV * (DK / 16), 1) verify_fold_pertoken_kernel
 __global__ void flush_lengths_kernel(int32_t *buf_len, const int32_t *state_idx, int B, int n_slot,
                                      int cap, int threshold, int force, int32_t *status)
 {
+    pdl_wait();
+    pdl_release();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
     const int slot = state_idx ? state_idx[b] : b;
@@ -289,6 +296,8 @@ __global__ void flush_lengths_kernel(int32_t *buf_len, const int32_t *state_idx,
 __global__ void accept_kernel(int32_t *buf_len, const int32_t *state_idx, const int32_t *accepted,
                               int B, int n_slot, int T, int cap, int32_t *status)
 {
+    pdl_wait();
+    pdl_release();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
     const int slot = state_idx ? state_idx[b] : b;
@@ -305,6 +314,8 @@ __global__ void accept_kernel(int32_t *buf_len, const int32_t *state_idx, const 
 __global__ void accept_fold_kernel(int32_t *buf_len, const int32_t *state_idx, const int32_t *accepted,
                                    int B, int n_slot, int T, int cap, int threshold, int32_t *status)
 {
+    pdl_wait();
+    pdl_release();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
     const int slot = state_idx ? state_idx[b] : b;
@@ -345,8 +356,8 @@ int launch_replay(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s)
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return GDN_ERR_LAUNCH;
     const int rows = MODE == kVerifyFold ? DV : kRows;
-    kern<<<dim3(d->H, d->B, DV / rows), rows * (DK / 16), smem, s>>>(a);
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+    return launch_pdl(kern, dim3(d->H, d->B, DV / rows), dim3(rows * (DK / 16)), smem, s, a) == cudaSuccess
+               ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
 template <int MODE>
@@ -398,9 +409,9 @@ int gdn_replay_accept(const gdn_replay_dims *d, int32_t *buf_len, const int32_t 
     if (rc) return rc;
     if (d->B == 0) return GDN_OK;
     if (!buf_len || !accepted || !status) return GDN_ERR_NULL;
-    accept_kernel<<<(d->B + 127) / 128, 128, 0, stream>>>(buf_len, state_idx, accepted, d->B,
-                                                           d->n_slot, d->T, d->cap, status);
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+    return launch_pdl(accept_kernel, dim3((d->B + 127) / 128), dim3(128), 0, stream, buf_len, state_idx,
+                      accepted, d->B, d->n_slot, d->T, d->cap, status) == cudaSuccess
+               ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
 int gdn_replay_flush(const gdn_replay_dims *d, float *state, const int32_t *state_idx,
@@ -423,9 +434,9 @@ int gdn_replay_flush(const gdn_replay_dims *d, float *state, const int32_t *stat
     int r = gdn::tc_flush(d, a, stream);
     if (r > 0) r = dispatch_replay<kFlush>(d, a, stream);
     if (r) return r;
-    flush_lengths_kernel<<<(d->B + 127) / 128, 128, 0, stream>>>(buf_len, state_idx, d->B, d->n_slot,
-                                                                  d->cap, d->threshold, a.force, status);
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+    return launch_pdl(flush_lengths_kernel, dim3((d->B + 127) / 128), dim3(128), 0, stream, buf_len,
+                      state_idx, d->B, d->n_slot, d->cap, d->threshold, a.force, status) == cudaSuccess
+               ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
 int gdn_replay_verify_fold(const gdn_replay_dims *d, float *state, const int32_t *state_idx,
@@ -450,7 +461,9 @@ int gdn_replay_verify_fold(const gdn_replay_dims *d, float *state, const int32_t
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = out; a.status = status;
     a.B = d->B; a.H = d->H; a.T = d->T; a.cap = d->cap; a.threshold = d->threshold;
     a.n_slot = d->n_slot; a.scale = d->scale;
-    const int tc = gdn::tc_verify(d, a, stream, true);
+    int tc = gdn::tc_verify_fold_split(d, a, stream);
+    if (tc <= 0) return tc;
+    tc = gdn::tc_verify(d, a, stream, true);
     if (tc <= 0) return tc;
     return dispatch_replay<kVerifyFold>(d, a, stream);
 }
@@ -462,9 +475,9 @@ int gdn_replay_accept_fold(const gdn_replay_dims *d, int32_t *buf_len, const int
     if (rc) return rc;
     if (d->B == 0) return GDN_OK;
     if (!buf_len || !accepted || !status) return GDN_ERR_NULL;
-    accept_fold_kernel<<<(d->B + 127) / 128, 128, 0, stream>>>(buf_len, state_idx, accepted, d->B, d->n_slot,
-                                                                d->T, d->cap, d->threshold, status);
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+    return launch_pdl(accept_fold_kernel, dim3((d->B + 127) / 128), dim3(128), 0, stream, buf_len, state_idx,
+                      accepted, d->B, d->n_slot, d->T, d->cap, d->threshold, status) == cudaSuccess
+               ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
 const char *gdn_replay_strerror(int code) {

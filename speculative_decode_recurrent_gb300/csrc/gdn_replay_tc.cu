@@ -72,6 +72,14 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         ::"r"(saddr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(saddr(bar))
         : "memory");
 }
+__device__ __forceinline__ void prefetch_tile_l2(const CUtensorMap *map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {   // 16-byte multiples
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+                 : "memory");
+}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -195,23 +203,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
 {
     const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
-    const int slot = a.state_idx ? a.state_idx[b] : b;
-    if (slot < 0 || slot >= a.n_slot) {
-        if (tid == 0 && h == 0) atomicOr(a.status, GDN_STATUS_BAD_SLOT);
-        return;
-    }
-    const int len = a.buf_len[slot];
     const int T = a.T, H = a.H, cap = a.cap;
-    const bool fold = FOLD && len >= a.threshold && len <= cap;
-    if (len < 0 || (!fold && len + T > cap)) {
-        if (tid == 0 && h == 0) atomicOr(a.status, len < 0 || len > cap ? GDN_STATUS_BAD_LEN : GDN_STATUS_NO_ROOM);
-        return;
-    }
-    const int C = len + T;                   // replayed tokens: buffer, then draft
-    const int NP = round16(C + T);           // rows of the [K;Q] operand
-    const int CP = round16(C);               // key columns of the K.K / Q.K product
-    const int LDA = CP + 4;
-    const int row0 = fold ? 0 : len;         // buffer slot of draft token 0
     const int cmax = FOLD ? cap + T : cap;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -231,11 +223,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     float *sGl = sGh + GS;
     float *sBeta = sGl + GS;
     float *sGam = sBeta + GS;
-    float *sMat = reinterpret_cast<float *>(sB);                  // reused after the MMAs
-    float *sPQ = sMat + static_cast<size_t>(C + T) * LDA;         // [T][128]
     uint8_t *sU = sA;                                             // fold: 3 x 16 KB
     uint8_t *sKt = sA + 49152;                                    // fold: 16 KB
 
+    // prologue that touches no global memory: overlaps the previous kernel
     if (tid == 0) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
@@ -247,6 +238,30 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();
+    pdl_release();
+
+    const int slot = a.state_idx ? a.state_idx[b] : b;
+    const int len = (slot >= 0 && slot < a.n_slot) ? a.buf_len[slot] : 0;
+    const bool fold = FOLD && len >= a.threshold && len <= cap;
+    int bad = 0;
+    if (slot < 0 || slot >= a.n_slot) bad = GDN_STATUS_BAD_SLOT;
+    else if (len < 0 || (!fold && len + T > cap)) bad = len < 0 || len > cap ? GDN_STATUS_BAD_LEN : GDN_STATUS_NO_ROOM;
+    // fold_class 2: only the folding units; the others belong to the launch that follows
+    const bool other_class = a.fold_class == 2 && !fold;
+    if (bad || other_class) {                                     // uniform across the CTA
+        if (bad && tid == 0 && h == 0) atomicOr(a.status, bad);
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+        return;
+    }
+    const int C = len + T;                   // replayed tokens: buffer, then draft
+    const int NP = round16(C + T);           // rows of the [K;Q] operand
+    const int CP = round16(C);               // key columns of the K.K / Q.K product
+    const int LDA = CP + 4;
+    const int row0 = fold ? 0 : len;         // buffer slot of draft token 0
+    float *sMat = reinterpret_cast<float *>(sB);                  // reused after the MMAs
+    float *sPQ = sMat + static_cast<size_t>(C + T) * LDA;         // [T][128]
 
     const size_t unit = static_cast<size_t>(slot) * H + h;
     const int ytile = static_cast<int>(unit) * 128;
@@ -254,6 +269,33 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
         mbar_expect_tx(&bar[0], 65536);
 #pragma unroll
         for (int kb = 0; kb < 4; ++kb) tma_load_2d(sA + kb * 16384, &tm_state, kb * 32, ytile, &bar[0]);
+    }
+
+    // ---- the unit that will run one wave later (CTA index + prefetch_stride): its
+    //      checkpoint tile, buffer rows and draft rows are prefetched into L2 now, so
+    //      the DRAM reads of that wave overlap this wave's compute
+    if (a.prefetch_stride > 0 && warp == 1) {
+        const int lane = tid & 31;
+        const int nxt = b * gridDim.x + h + a.prefetch_stride;
+        if (nxt < static_cast<int>(gridDim.x * gridDim.y)) {
+            const int nb = nxt / gridDim.x, nh = nxt % gridDim.x;
+            const int ns = a.state_idx ? a.state_idx[nb] : nb;
+            if (ns >= 0 && ns < a.n_slot) {
+                const int nlen = min(max(a.buf_len[ns], 0), cap);
+                const size_t nunit = static_cast<size_t>(ns) * H + nh;
+                if (lane < 4) prefetch_tile_l2(&tm_state, lane * 32, static_cast<int>(nunit) * 128);
+                if (lane == 4 && nlen > 0)
+                    prefetch_l2(reinterpret_cast<const __nv_bfloat16 *>(a.buf_k) + nunit * cap * 128, nlen * 256);
+                if (lane == 5 && nlen > 0)
+                    prefetch_l2(reinterpret_cast<const __nv_bfloat16 *>(a.buf_v) + nunit * cap * 128, nlen * 256);
+                const size_t nrow0 = (static_cast<size_t>(nb) * T * H + nh) * 128;
+                for (int r = lane; r < 3 * T; r += 32) {           // draft k, q, v rows (256 B each)
+                    const void *base3 = r < T ? a.k : r < 2 * T ? a.q : a.v;
+                    prefetch_l2(reinterpret_cast<const __nv_bfloat16 *>(base3) + nrow0 +
+                                    static_cast<size_t>(r % T) * H * 128, 256);
+                }
+            }
+        }
     }
 
     // ---- every global load of this unit, issued back to back (one memory latency)
@@ -278,15 +320,26 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
             raw[i] = __ldg(reinterpret_cast<const uint4 *>(src) + c);
         }
     }
-    // value channel `tid` of every token: unconditional loads from clamped addresses so
-    // that all of them are in flight together; widened to fp32 only when first used
-    unsigned short vraw[CMAX];
+    // value rows as 16-byte vectors (moved through shared memory once the S0 tile is free)
+    constexpr int NVV = CMAX * 16 / kThreads;
+    uint4 vload[NVV];
 #pragma unroll
-    for (int t = 0; t < CMAX; ++t) {
-        const int tc = t < C ? t : C - 1;
-        const __nv_bfloat16 *vp = tc < len ? bv + static_cast<size_t>(tc) * 128
-                                           : dv + static_cast<size_t>(tc - len) * dstride;
-        vraw[t] = __ldg(reinterpret_cast<const unsigned short *>(vp) + tid);
+    for (int i = 0; i < NVV; ++i) {
+        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+        if (r < C) {
+            const __nv_bfloat16 *src = r < len ? bv + static_cast<size_t>(r) * 128
+                                               : dv + static_cast<size_t>(r - len) * dstride;
+            vload[i] = __ldg(reinterpret_cast<const uint4 *>(src) + c);
+        }
+    }
+    // fold: the draft keys are re-staged at slot 0 after every buffer read is done
+    uint4 kdraft[2];
+    if (fold) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+            if (r < T) kdraft[i] = __ldg(reinterpret_cast<const uint4 *>(dk + static_cast<size_t>(r) * dstride) + c);
+        }
     }
     float gq[2] = {0.f, 0.f}, bq[2] = {0.f, 0.f};                 // gates of tokens lane, lane + 32 (warp 0)
     if (warp == 0) {
@@ -358,13 +411,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
                     a.buf_beta[unit * cap + t] = bq[i];
                 }
             }
-        }
-    }
-    if (!fold) {
-        for (int e = tid; e < T * 16; e += kThreads) {            // draft values into the buffer
-            const int r = e >> 4, c = e & 15;
-            reinterpret_cast<uint4 *>(wv + static_cast<size_t>(r) * 128)[c] =
-                __ldg(reinterpret_cast<const uint4 *>(dv + static_cast<size_t>(r) * dstride) + c);
         }
     }
     fence_proxy_async();                      // generic writes of the [K;Q] tile -> async proxy
@@ -468,6 +514,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
         const uint8_t *colbase = sB + (tid >> 5) * NP * 128 + (tid & 3) * 4;
 #pragma unroll
         for (int c8 = 0; c8 < CMAX / 8; ++c8) {
+            if (c8 * 8 >= round16(len)) break;                   // the MMA reads round16(len) tokens
             __nv_bfloat16 kk[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -478,6 +525,38 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
             }
             *reinterpret_cast<uint4 *>(sKt + sw128(tid, c8)) =
                 make_uint4(pack2(kk[0], kk[1]), pack2(kk[2], kk[3]), pack2(kk[4], kk[5]), pack2(kk[6], kk[7]));
+        }
+    }
+    // park the value rows in the free S0 tile; once every thread has its loads back
+    // (the barrier), no read of the old buffer is outstanding and the draft (k, v, g,
+    // beta) can be staged into slots row0 .. row0 + T - 1
+    __nv_bfloat16 *sV = reinterpret_cast<__nv_bfloat16 *>(sA);   // [C][128] bf16
+#pragma unroll
+    for (int i = 0; i < NVV; ++i) {
+        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+        if (r < C) reinterpret_cast<uint4 *>(sV + static_cast<size_t>(r) * 128)[c] = vload[i];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < NVV; ++i) {
+        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+        if (r >= len && r < C) reinterpret_cast<uint4 *>(wv + static_cast<size_t>(r - len) * 128)[c] = vload[i];
+    }
+    if (fold) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+            if (r < T) reinterpret_cast<uint4 *>(wk + static_cast<size_t>(r) * 128)[c] = kdraft[i];
+        }
+        if (warp == 0) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int t = (tid & 31) + 32 * i;
+                if (t >= len && t < C) {
+                    a.buf_g[unit * cap + (t - len)] = gq[i];
+                    a.buf_beta[unit * cap + (t - len)] = bq[i];
+                }
+            }
         }
     }
     __syncthreads();                                              // [K;Q] tile no longer read
@@ -523,15 +602,17 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
             c2 = fmaf(a4.z, u[s + 2], c2);
             c3 = fmaf(a4.w, u[s + 3], c3);
         }
-        const float vt = __bfloat162float(__ushort_as_bfloat16(vraw[t]));
+        const float vt = __bfloat162float(sV[static_cast<size_t>(t) * 128 + tid]);
         u[t] = sBeta[t] * (vt - sGam[t] * pc[t & 15]) - ((c0 + c1) + (c2 + c3));
     }
     // ---- fold: U~_s = e^{G_{len-1} - G_s} u_s (s < len) as three bf16 tiles, then
     //      D = U~^T K on the tensor cores while the outputs below run on the ALUs
     if (fold) {
         const float gh = sGh[len - 1], gl = sGl[len - 1];
+        __syncthreads();                                          // value rows (in sA) fully read
 #pragma unroll
         for (int c8 = 0; c8 < CMAX / 8; ++c8) {
+            if (c8 * 8 >= round16(len)) break;                   // the MMA reads round16(len) tokens
             __nv_bfloat16 hh[8], mm[8], ll[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -623,24 +704,458 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
             for (int kb = 0; kb < 4; ++kb) tma_store_2d(&tm_state, kb * 32, ytile, sA + kb * 16384);
             tma_store_commit_and_wait();
         }
-        // ---- the draft becomes buffer tokens 0 .. T-1 (every read of the old buffer is done)
-        for (int e = tid; e < T * 16; e += kThreads) {
-            const int r = e >> 4, c = e & 15;
-            reinterpret_cast<uint4 *>(wk + static_cast<size_t>(r) * 128)[c] =
-                __ldg(reinterpret_cast<const uint4 *>(dk + static_cast<size_t>(r) * dstride) + c);
-            reinterpret_cast<uint4 *>(wv + static_cast<size_t>(r) * 128)[c] =
-                __ldg(reinterpret_cast<const uint4 *>(dv + static_cast<size_t>(r) * dstride) + c);
-        }
-        for (int t = tid; t < T; t += kThreads) {
-            const size_t gi = (static_cast<size_t>(b) * T + t) * H + h;
-            a.buf_g[unit * cap + t] = a.g[gi];
-            a.buf_beta[unit * cap + t] = a.beta[gi];
-        }
     }
 
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// Four-CTA verify (no fold; cap <= 48, T <= 16).  Two CTAs per SM leave the SM idle
+// once the first wave's loads are in; with 128 TMEM columns, at most ~50 KB of shared
+// memory and 128 registers per thread, four CTAs fit on an SM and the whole decode
+// batch runs in one wave.  The checkpoint streams through in two K-halves of 64
+// columns (32 KB), each followed by its half of the S0 [K;Q]^T and [K;Q] K^T MMAs.
+//
+// Shared-memory plan (bytes from the 1024-aligned base):
+//   [0, SB)          [K;Q] fp32, one K-half at a time: 2 sub-tiles of NPmax rows x 128 B
+//   [SB, SB + 32K)   S0, one K-half at a time (TMA): 2 sub-tiles of 128 rows x 128 B.
+//                    An M = 128 operand starting in the [K;Q] tile reads on into this
+//                    tile; those rows feed accumulator lanes that are never read.
+//   after both halves the same bytes hold the value rows (bf16, [C][128]), the
+//   coefficient matrices (row stride CP + 4) and the S0 q columns ([T][128])
+//   then: 4 mbarriers, TMEM slot, flag, G (hi, lo), beta, gamma per token.
+constexpr int kTmemCols4 = 128;
+__host__ __device__ inline int v4_sb_bytes(int cap, int T) { return 2 * round16(cap + T) * 128; }
+__host__ __device__ inline int v4_region_bytes(int cap, int T) {
+    const int tiles = v4_sb_bytes(cap, T) + 32768;
+    const int need = cap * 256 + (cap + T) * (round16(cap) + 4) * 4 + T * 512;
+    return tiles > need ? tiles : ((need + 1023) & ~1023);
+}
+__host__ __device__ inline int v4_smem_bytes(int cap, int T) { return v4_region_bytes(cap, T) + 64 + 16 * round16(cap); }
+
+template <int CMAX>
+__global__ void __launch_bounds__(kThreads, 4)
+verify4_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
+{
+    const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+    const int T = a.T, H = a.H, cap = a.cap;
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (saddr(smem_raw) & 1023u) {           // the swizzled tiles need a 1024-byte aligned base
+        if (tid == 0) atomicOr(a.status, kStatusTimeout);
+        return;
+    }
+    uint8_t *sB = smem_raw;
+    uint8_t *sA = smem_raw + v4_sb_bytes(cap, T);
+    uint8_t *sm = smem_raw + v4_region_bytes(cap, T);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm);            // TMA (2 phases), MMA half 0, K.K, P
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + 32);
+    int *flag = reinterpret_cast<int *>(sm + 36);
+    const int GS = round16(cap);
+    float *sGh = reinterpret_cast<float *>(sm + 64);
+    float *sGl = sGh + GS;
+    float *sBeta = sGl + GS;
+    float *sGam = sBeta + GS;
+
+    if (tid == 0) {                                               // prologue: no global memory
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
+        *flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, kTmemCols4);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // fold_class 1: this launch runs beside the fold launch that precedes it and must
+    // not wait for it (every CTA of that launch has waited for the earlier kernels
+    // before letting this one start); CTA (0, 0) waits for it at the end instead, so
+    // the following kernel still observes both launches as complete.
+    const bool split = a.fold_class == 1;
+    const bool waiter = split && blockIdx.x == 0 && blockIdx.y == 0;
+    if (!split) pdl_wait();
+
+    const int slot = a.state_idx ? a.state_idx[b] : b;
+    const int len = (slot >= 0 && slot < a.n_slot) ? a.buf_len[slot] : 0;
+    int bad = 0;
+    const bool other_class = split && len >= a.threshold && len <= cap;   // the fold launch's unit
+    if (slot < 0 || slot >= a.n_slot) bad = GDN_STATUS_BAD_SLOT;
+    else if (!other_class && (len < 0 || len + T > cap))
+        bad = len < 0 || len > cap ? GDN_STATUS_BAD_LEN : GDN_STATUS_NO_ROOM;
+    pdl_release();                                                // every length of this CTA is read
+    if (bad || other_class) {                                     // uniform across the CTA
+        if (bad && tid == 0 && h == 0 && !split) atomicOr(a.status, bad);
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tmem, kTmemCols4);
+        if (waiter) pdl_wait();
+        return;
+    }
+    const int C = len + T;
+    const int NP = round16(C + T);
+    const int CP = round16(C);
+    const int LDA = CP + 4;
+
+    const size_t unit = static_cast<size_t>(slot) * H + h;
+    const int ytile = static_cast<int>(unit) * 128;
+    if (tid == 0) {                                               // S0 columns 0..63; 64..127 into L2
+        mbar_expect_tx(&bar[0], 32768);
+        tma_load_2d(sA, &tm_state, 0, ytile, &bar[0]);
+        tma_load_2d(sA + 16384, &tm_state, 32, ytile, &bar[0]);
+        prefetch_tile_l2(&tm_state, 64, ytile);
+        prefetch_tile_l2(&tm_state, 96, ytile);
+    }
+    if (a.prefetch_stride > 0 && warp == 1) {                     // the unit one wave later -> L2
+        const int lane = tid & 31;
+        const int nxt = b * gridDim.x + h + a.prefetch_stride;
+        if (nxt < static_cast<int>(gridDim.x * gridDim.y)) {
+            const int nb = nxt / gridDim.x, nh = nxt % gridDim.x;
+            const int ns = a.state_idx ? a.state_idx[nb] : nb;
+            if (ns >= 0 && ns < a.n_slot) {
+                const int nlen = min(max(a.buf_len[ns], 0), cap);
+                const size_t nunit = static_cast<size_t>(ns) * H + nh;
+                if (lane < 4) prefetch_tile_l2(&tm_state, lane * 32, static_cast<int>(nunit) * 128);
+                if (lane == 4 && nlen > 0)
+                    prefetch_l2(reinterpret_cast<const __nv_bfloat16 *>(a.buf_k) + nunit * cap * 128, nlen * 256);
+                if (lane == 5 && nlen > 0)
+                    prefetch_l2(reinterpret_cast<const __nv_bfloat16 *>(a.buf_v) + nunit * cap * 128, nlen * 256);
+                const size_t nrow0 = (static_cast<size_t>(nb) * T * H + nh) * 128;
+                for (int r = lane; r < 3 * T; r += 32) {
+                    const void *base3 = r < T ? a.k : r < 2 * T ? a.q : a.v;
+                    prefetch_l2(reinterpret_cast<const __nv_bfloat16 *>(base3) + nrow0 +
+                                    static_cast<size_t>(r % T) * H * 128, 256);
+                }
+            }
+        }
+    }
+
+    // ---- every global load of this unit, issued back to back
+    const __nv_bfloat16 *bk = reinterpret_cast<const __nv_bfloat16 *>(a.buf_k) + unit * cap * 128;
+    const __nv_bfloat16 *bv = reinterpret_cast<const __nv_bfloat16 *>(a.buf_v) + unit * cap * 128;
+    const size_t drow0 = (static_cast<size_t>(b) * T * H + h) * 128;
+    const size_t dstride = static_cast<size_t>(H) * 128;
+    const __nv_bfloat16 *dk = reinterpret_cast<const __nv_bfloat16 *>(a.k) + drow0;
+    const __nv_bfloat16 *dq = reinterpret_cast<const __nv_bfloat16 *>(a.q) + drow0;
+    const __nv_bfloat16 *dv = reinterpret_cast<const __nv_bfloat16 *>(a.v) + drow0;
+    __nv_bfloat16 *wk = reinterpret_cast<__nv_bfloat16 *>(a.buf_k) + (unit * cap + len) * 128;
+    __nv_bfloat16 *wv = reinterpret_cast<__nv_bfloat16 *>(a.buf_v) + (unit * cap + len) * 128;
+    constexpr int NV = (CMAX + 16) * 16 / kThreads;
+    uint4 raw[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+        if (r < C + T) {
+            const __nv_bfloat16 *src = r < len ? bk + static_cast<size_t>(r) * 128
+                                     : r < C   ? dk + static_cast<size_t>(r - len) * dstride
+                                               : dq + static_cast<size_t>(r - C) * dstride;
+            raw[i] = __ldg(reinterpret_cast<const uint4 *>(src) + c);
+        }
+    }
+    constexpr int NVV = CMAX * 16 / kThreads;
+    uint4 vload[NVV];
+#pragma unroll
+    for (int i = 0; i < NVV; ++i) {
+        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+        if (r < C) {
+            const __nv_bfloat16 *src = r < len ? bv + static_cast<size_t>(r) * 128
+                                               : dv + static_cast<size_t>(r - len) * dstride;
+            vload[i] = __ldg(reinterpret_cast<const uint4 *>(src) + c);
+        }
+    }
+    float gq[2] = {0.f, 0.f}, bq[2] = {0.f, 0.f};
+    if (warp == 0) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int t = (tid & 31) + 32 * i;
+            if (t < C) {
+                if (t < len) {
+                    gq[i] = a.buf_g[unit * cap + t];
+                    bq[i] = a.buf_beta[unit * cap + t];
+                } else {
+                    const size_t gi = (static_cast<size_t>(b) * T + (t - len)) * H + h;
+                    gq[i] = a.g[gi];
+                    bq[i] = a.beta[gi];
+                }
+            }
+        }
+    }
+    // ---- K-half 0 of [K;Q] (columns 0..63) into the swizzled fp32 tile; draft keys
+    //      and values into the buffer (slots len .. len + T - 1, never read here)
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+        if (r < C + T) {
+            if (r >= len && r < C) reinterpret_cast<uint4 *>(wk + static_cast<size_t>(r - len) * 128)[c] = raw[i];
+            if (c < 8) {
+                float f[8];
+                bf16x8_to_f32(raw[i], f);
+                uint8_t *tile = sB + (c >> 2) * NP * 128;
+                const int ch = (c & 3) * 2;
+                *reinterpret_cast<float4 *>(tile + sw128(r, ch)) = make_float4(f[0], f[1], f[2], f[3]);
+                *reinterpret_cast<float4 *>(tile + sw128(r, ch + 1)) = make_float4(f[4], f[5], f[6], f[7]);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NVV; ++i) {
+        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+        if (r >= len && r < C) reinterpret_cast<uint4 *>(wv + static_cast<size_t>(r - len) * 128)[c] = vload[i];
+    }
+    if (warp == 0) {                                              // compensated scan of g
+        const int lane = tid & 31;
+        float hi[2], lo[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            hi[i] = gq[i];
+            lo[i] = 0.f;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float h2 = __shfl_up_sync(0xffffffffu, hi[i], off);
+                const float l2 = __shfl_up_sync(0xffffffffu, lo[i], off);
+                if (lane >= off) {
+                    const float s1 = hi[i] + h2, bp = s1 - hi[i];
+                    lo[i] += l2 + ((hi[i] - (s1 - bp)) + (h2 - bp));
+                    hi[i] = s1;
+                }
+            }
+        }
+        const float chh = __shfl_sync(0xffffffffu, hi[0], 31), cll = __shfl_sync(0xffffffffu, lo[0], 31);
+        {
+            const float s1 = hi[1] + chh, bp = s1 - hi[1];
+            lo[1] += cll + ((hi[1] - (s1 - bp)) + (chh - bp));
+            hi[1] = s1;
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int t = lane + 32 * i;
+            if (t < C) {
+                sGh[t] = hi[i];
+                sGl[t] = lo[i];
+                sGam[t] = __expf(hi[i] + lo[i]);
+                sBeta[t] = bq[i];
+                if (t >= len) {
+                    a.buf_g[unit * cap + t] = gq[i];
+                    a.buf_beta[unit * cap + t] = bq[i];
+                }
+            }
+        }
+    }
+    fence_proxy_async();
+    __syncthreads();
+    const uint32_t idP = idesc_mn(2, 128, NP), idK = idesc_mn(2, 128, CP);
+    const uint32_t a0 = saddr(sA), b0 = saddr(sB);
+    if (tid == 0) {
+        if (mbar_wait(&bar[0], 0)) {
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {                       // K-half 0: 8 steps of 8 columns
+                const uint32_t off = (ks & 3) * 32;
+                const uint64_t db = desc_sw128(b0 + (ks >> 2) * NP * 128 + off);
+                mma_tf32(tmem + NP, db, db, idK, ks > 0);
+                mma_tf32(tmem, desc_sw128(a0 + (ks >> 2) * 16384 + off), db, idP, ks > 0);
+            }
+            mma_commit(&bar[1]);
+        } else {
+            *flag = 1;
+        }
+    }
+    __syncthreads();
+    bool ok = *flag == 0;
+    if (ok) ok = mbar_wait(&bar[1], 0);
+    if (__syncthreads_or(!ok)) {
+        if (tid == 0) {
+            mbar_wait(&bar[0], 0);
+            if (*flag == 0) mbar_wait(&bar[1], 0);
+            atomicOr(a.status, kStatusTimeout);
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tmem, kTmemCols4);
+        if (waiter) pdl_wait();
+        return;
+    }
+    tc_fence_after();
+    // ---- K-half 1: S0 columns 64..127 (L2-warm) and [K;Q] columns 64..127
+    if (tid == 0) {
+        mbar_expect_tx(&bar[0], 32768);
+        tma_load_2d(sA, &tm_state, 64, ytile, &bar[0]);
+        tma_load_2d(sA + 16384, &tm_state, 96, ytile, &bar[0]);
+    }
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+        if (r < C + T && c >= 8) {
+            float f[8];
+            bf16x8_to_f32(raw[i], f);
+            uint8_t *tile = sB + ((c - 8) >> 2) * NP * 128;
+            const int ch = (c & 3) * 2;
+            *reinterpret_cast<float4 *>(tile + sw128(r, ch)) = make_float4(f[0], f[1], f[2], f[3]);
+            *reinterpret_cast<float4 *>(tile + sw128(r, ch + 1)) = make_float4(f[4], f[5], f[6], f[7]);
+        }
+    }
+    fence_proxy_async();
+    __syncthreads();
+    if (tid == 0) {
+        if (mbar_wait(&bar[0], 1)) {
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint64_t db = desc_sw128(b0 + (ks >> 2) * NP * 128 + (ks & 3) * 32);
+                mma_tf32(tmem + NP, db, db, idK, 1);
+            }
+            mma_commit(&bar[2]);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t off = (ks & 3) * 32;
+                mma_tf32(tmem, desc_sw128(a0 + (ks >> 2) * 16384 + off),
+                         desc_sw128(b0 + (ks >> 2) * NP * 128 + off), idP, 1);
+            }
+            mma_commit(&bar[3]);
+        } else {
+            *flag = 1;
+        }
+    }
+    __syncthreads();
+    ok = *flag == 0;
+    if (ok) ok = mbar_wait(&bar[2], 0);
+    if (__syncthreads_or(!ok)) {
+        if (tid == 0) {
+            mbar_wait(&bar[0], 1);
+            if (*flag == 0) {
+                mbar_wait(&bar[2], 0);
+                mbar_wait(&bar[3], 0);
+            }
+            atomicOr(a.status, kStatusTimeout);
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tmem, kTmemCols4);
+        if (waiter) pdl_wait();
+        return;
+    }
+    tc_fence_after();
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    // ---- coefficient rows (registers until the P MMA has released the tiles)
+    float m[CMAX / 16][16];
+    {
+        const bool is_q = tid >= C;
+        const int p = tid >= C + T ? C - 1 : is_q ? len + (tid - C) : tid;
+        const float gh = sGh[p], gl = sGl[p];
+        const float scl = is_q ? 1.f : sBeta[p];
+        const int lim = tid >= C + T ? 0 : is_q ? min(p + 1, C) : tid;
+#pragma unroll
+        for (int cb = 0; cb < CMAX / 16; ++cb) {
+            const int c0 = cb * 16;
+            if (c0 >= CP) break;
+            float kq[16];
+            tmem_ld16(lane_base + NP + c0, kq);
+            float gs[16], ls[16];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float4 x = *reinterpret_cast<const float4 *>(sGh + c0 + 4 * j);
+                const float4 y = *reinterpret_cast<const float4 *>(sGl + c0 + 4 * j);
+                gs[4 * j] = x.x; gs[4 * j + 1] = x.y; gs[4 * j + 2] = x.z; gs[4 * j + 3] = x.w;
+                ls[4 * j] = y.x; ls[4 * j + 1] = y.y; ls[4 * j + 2] = y.z; ls[4 * j + 3] = y.w;
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float e = __expf((gh - gs[j]) + (gl - ls[j]));
+                m[cb][j] = (c0 + j < lim) ? scl * e * kq[j] : 0.f;
+            }
+        }
+    }
+    ok = mbar_wait(&bar[3], 0);
+    if (__syncthreads_or(!ok)) {
+        if (tid == 0) {
+            mbar_wait(&bar[3], 0);
+            atomicOr(a.status, kStatusTimeout);
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tmem, kTmemCols4);
+        if (waiter) pdl_wait();
+        return;
+    }
+    tc_fence_after();
+    float pq[2][16];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int c0 = (C & ~15) + 16 * i;
+        if (c0 < C + T) tmem_ld16(lane_base + c0, pq[i]);
+    }
+    // the tiles are free: value rows, coefficient rows and S0 q columns take their place
+    __nv_bfloat16 *sV = reinterpret_cast<__nv_bfloat16 *>(smem_raw);          // [C][128]
+    float *sMat = reinterpret_cast<float *>(smem_raw + static_cast<size_t>(C) * 256);
+    float *sPQ = sMat + static_cast<size_t>(C + T) * LDA;                     // [T][128]
+#pragma unroll
+    for (int i = 0; i < NVV; ++i) {
+        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+        if (r < C) reinterpret_cast<uint4 *>(sV + static_cast<size_t>(r) * 128)[c] = vload[i];
+    }
+    if (tid < C + T) {
+#pragma unroll
+        for (int cb = 0; cb < CMAX / 16; ++cb) {
+            if (cb * 16 >= CP) break;
+            float4 *dst = reinterpret_cast<float4 *>(sMat + static_cast<size_t>(tid) * LDA + cb * 16);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                dst[j] = make_float4(m[cb][4 * j], m[cb][4 * j + 1], m[cb][4 * j + 2], m[cb][4 * j + 3]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int t = (C & ~15) + 16 * i + j;
+            if (t >= C && t < C + T) sPQ[static_cast<size_t>(t - C) * 128 + tid] = pq[i][j];
+        }
+    }
+    __syncthreads();
+    // ---- forward substitution, one state row per thread (see the two-CTA kernel)
+    float u[CMAX];
+    float pc[16];
+#pragma unroll
+    for (int t = 0; t < CMAX; ++t) u[t] = 0.f;
+#pragma unroll
+    for (int t = 0; t < CMAX; ++t) {
+        if (t >= C) break;
+        if ((t & 15) == 0) tmem_ld16(lane_base + t, pc);
+        const float *Ar = sMat + static_cast<size_t>(t) * LDA;
+        float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+#pragma unroll
+        for (int s = 0; s < t; s += 4) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(Ar + s);
+            c0 = fmaf(a4.x, u[s], c0);
+            c1 = fmaf(a4.y, u[s + 1], c1);
+            c2 = fmaf(a4.z, u[s + 2], c2);
+            c3 = fmaf(a4.w, u[s + 3], c3);
+        }
+        const float vt = __bfloat162float(sV[static_cast<size_t>(t) * 128 + tid]);
+        u[t] = sBeta[t] * (vt - sGam[t] * pc[t & 15]) - ((c0 + c1) + (c2 + c3));
+    }
+    // ---- draft outputs
+    for (int t2 = 0; t2 < T; ++t2) {
+        const int p = len + t2;
+        const float *Mr = sMat + static_cast<size_t>(C + t2) * LDA;
+        float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+#pragma unroll
+        for (int s = 0; s < CMAX; s += 4) {
+            if ((s & 15) == 0 && s > p) break;
+            const float4 m4 = *reinterpret_cast<const float4 *>(Mr + s);
+            c0 = fmaf(m4.x, u[s], c0);
+            c1 = fmaf(m4.y, u[s + 1], c1);
+            c2 = fmaf(m4.z, u[s + 2], c2);
+            c3 = fmaf(m4.w, u[s + 3], c3);
+        }
+        const float o = sGam[p] * sPQ[static_cast<size_t>(t2) * 128 + tid] + ((c0 + c1) + (c2 + c3));
+        a.out[((static_cast<size_t>(b) * T + t2) * H + h) * 128 + tid] = a.scale * o;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols4);
+    if (waiter) pdl_wait();
 }
 
 // Shared-memory plan of the flush kernel (bytes from the 1024-aligned base):
@@ -657,15 +1172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 flush_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
 {
     const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
-    const int slot = a.state_idx ? a.state_idx[b] : b;
-    if (slot < 0 || slot >= a.n_slot) return;                      // reported by the length kernel
-    const int len = a.buf_len[slot];
     const int H = a.H, cap = a.cap;
-    if (len < 0 || len > cap) return;                               // reported by the length kernel
-    if (!(len >= a.threshold || (a.force && len > 0))) return;
-    const int C = len;
-    const int CP = round16(C);
-    const int LDA = CP + 4;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -684,6 +1191,17 @@ flush_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a
     float *sGl = sGh + GS;
     float *sBeta = sGl + GS;
     float *sGam = sBeta + GS;
+
+    pdl_wait();
+    pdl_release();
+    const int slot = a.state_idx ? a.state_idx[b] : b;
+    if (slot < 0 || slot >= a.n_slot) return;                      // reported by the length kernel
+    const int len = a.buf_len[slot];
+    if (len < 0 || len > cap) return;                               // reported by the length kernel
+    if (!(len >= a.threshold || (a.force && len > 0))) return;
+    const int C = len;
+    const int CP = round16(C);
+    const int LDA = CP + 4;
 
     if (tid == 0) {
         mbar_init(&bar[0], 1);
@@ -1007,14 +1525,41 @@ bool state_map(CUtensorMap *m, const float *state, int rows) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int CMAX, bool FOLD>
-int launch_verify(const gdn_replay_dims *d, const ReplayArgs &a, const CUtensorMap &m, cudaStream_t s) {
-    const int smem = verify_smem_bytes(FOLD ? d->cap + d->T : d->cap, d->T);
-    auto kern = verify_tc_kernel<CMAX, FOLD>;
+// CTAs of one launch that can be resident at once (the prefetch distance).
+int resident_ctas(const void *kern, int smem) {
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess)
+        return 0;
+    return sms * per_sm;
+}
+
+int launch_verify4(const gdn_replay_dims *d, const ReplayArgs &a0, const CUtensorMap &m, cudaStream_t s) {
+    const int smem = v4_smem_bytes(d->cap, d->T);
+    auto kern = verify4_tc_kernel<48>;
+    static int stride = -1;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return GDN_ERR_LAUNCH;
-    kern<<<dim3(d->H, d->B), kThreads, smem, s>>>(m, a);
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+    if (stride < 0) stride = resident_ctas(reinterpret_cast<const void *>(kern), smem);
+    ReplayArgs a = a0;
+    a.prefetch_stride = stride;
+    return launch_pdl(kern, dim3(d->H, d->B), dim3(kThreads), smem, s, m, a) == cudaSuccess ? GDN_OK
+                                                                                       : GDN_ERR_LAUNCH;
+}
+
+template <int CMAX, bool FOLD>
+int launch_verify(const gdn_replay_dims *d, const ReplayArgs &a0, const CUtensorMap &m, cudaStream_t s) {
+    const int smem = verify_smem_bytes(FOLD ? d->cap + d->T : d->cap, d->T);
+    auto kern = verify_tc_kernel<CMAX, FOLD>;
+    static int stride = -1;                                       // per instantiation, per process
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return GDN_ERR_LAUNCH;
+    if (stride < 0) stride = resident_ctas(reinterpret_cast<const void *>(kern), smem);
+    ReplayArgs a = a0;
+    a.prefetch_stride = stride;
+    return launch_pdl(kern, dim3(d->H, d->B), dim3(kThreads), smem, s, m, a) == cudaSuccess ? GDN_OK
+                                                                                       : GDN_ERR_LAUNCH;
 }
 
 }  // namespace
@@ -1026,8 +1571,25 @@ int tc_verify(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s, boo
     if (verify_smem_bytes(cmax, d->T) > 227 * 1024) return 1;
     CUtensorMap m;
     if (!state_map(&m, a.state_in, d->n_slot * d->H * 128)) return 1;
+    if (!fold && d->cap <= 48) return launch_verify4(d, a, m, s);
     if (fold) return cmax <= 48 ? launch_verify<48, true>(d, a, m, s) : launch_verify<64, true>(d, a, m, s);
     return cmax <= 48 ? launch_verify<48, false>(d, a, m, s) : launch_verify<64, false>(d, a, m, s);
+}
+
+int tc_verify_fold_split(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s) {
+    if (d->dk != 128 || d->dv != 128 || d->in_dtype != GDN_DTYPE_BF16) return 1;
+    const int cmax = d->cap + d->T;
+    if (cmax > 64 || d->T > 16 || d->cap > 48) return 1;
+    if (verify_smem_bytes(cmax, d->T) > 227 * 1024) return 1;
+    CUtensorMap m;
+    if (!state_map(&m, a.state_in, d->n_slot * d->H * 128)) return 1;
+    ReplayArgs af = a;
+    af.fold_class = 2;                                            // folding units, waits for earlier kernels
+    int rc = cmax <= 48 ? launch_verify<48, true>(d, af, m, s) : launch_verify<64, true>(d, af, m, s);
+    if (rc) return rc;
+    ReplayArgs an = a;
+    an.fold_class = 1;                                            // the rest, beside the fold launch
+    return launch_verify4(d, an, m, s);
 }
 
 int tc_flush(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s) {
@@ -1039,8 +1601,8 @@ int tc_flush(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s) {
     auto kern = d->cap <= 48 ? flush_tc_kernel<48> : flush_tc_kernel<64>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return GDN_ERR_LAUNCH;
-    kern<<<dim3(d->H, d->B), kThreads, smem, s>>>(m, a);
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+    return launch_pdl(kern, dim3(d->H, d->B), dim3(kThreads), smem, s, m, a) == cudaSuccess ? GDN_OK
+                                                                                       : GDN_ERR_LAUNCH;
 }
 
 }  // namespace gdn

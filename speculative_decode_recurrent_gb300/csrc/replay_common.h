@@ -23,7 +23,33 @@ struct ReplayArgs {
     int32_t *status;
     int B, H, T, cap, threshold, force, n_slot;
     float scale;
+    int prefetch_stride;        // > 0: CTA i prefetches into L2 the unit of CTA i + stride
+    int fold_class;             // 0: all units; 2: only units that fold; 1: only units that do not
+                                // fold, launched beside a fold_class 2 launch
 };
+
+// Programmatic dependent launch: every kernel of the library is launched with
+// programmatic stream serialisation, waits (griddepcontrol.wait) before its first
+// read of global memory another kernel may have written, and then lets the next
+// kernel on the stream start its launch and prologue (launch_dependents).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 
 // Internal status bit: a bounded wait in a tensor-core kernel gave up (the
 // affected unit is skipped; nothing hangs).
@@ -36,5 +62,8 @@ constexpr int32_t kStatusTimeout = GDN_STATUS_TIMEOUT;
 // after their buffered tokens and stage the draft at buffer slot 0.
 int tc_verify(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s, bool fold);
 int tc_flush(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s);
+// Verify with fold as two launches on one stream: the folding sequences (two-CTA
+// kernel) and, running beside it, every other sequence (four-CTA kernel).
+int tc_verify_fold_split(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s);
 
 }  // namespace gdn
