@@ -191,7 +191,7 @@ __device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
 // and skips the unit.
 __host__ __device__ inline int verify_sb_bytes(int cmax, int T) { return (3 * round16(cmax + T) + 128) * 128; }
 __host__ __device__ inline int verify_smem_bytes(int cmax, int T) {
-    return 65536 + verify_sb_bytes(cmax, T) + 64 + 16 * round16(cmax);
+    return 65536 + verify_sb_bytes(cmax, T) + 64 + 20 * round16(cmax);
 }
 
 // FOLD = false: gdn_replay_verify.  FOLD = true: gdn_replay_verify_fold -- a unit whose
@@ -223,6 +223,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     float *sGl = sGh + GS;
     float *sBeta = sGl + GS;
     float *sGam = sBeta + GS;
+    float *sFold = sGam + GS;                                     // e^{G_{len-1} - G_s}, folding units
     uint8_t *sU = sA;                                             // fold: 3 x 16 KB
     uint8_t *sKt = sA + 49152;                                    // fold: 16 KB
 
@@ -559,6 +560,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
             }
         }
     }
+    if (fold && warp == 0) {                                      // fold factors, shared by all rows
+        const float gh = sGh[len - 1], gl = sGl[len - 1];
+        for (int t = tid; t < round16(len); t += 32)
+            sFold[t] = t < len ? __expf((gh - sGh[t]) + (gl - sGl[t])) : 0.f;
+    }
     __syncthreads();                                              // [K;Q] tile no longer read
     if (tid < C + T) {
 #pragma unroll
@@ -608,18 +614,16 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     // ---- fold: U~_s = e^{G_{len-1} - G_s} u_s (s < len) as three bf16 tiles, then
     //      D = U~^T K on the tensor cores while the outputs below run on the ALUs
     if (fold) {
-        const float gh = sGh[len - 1], gl = sGl[len - 1];
         __syncthreads();                                          // value rows (in sA) fully read
 #pragma unroll
         for (int c8 = 0; c8 < CMAX / 8; ++c8) {
             if (c8 * 8 >= round16(len)) break;                   // the MMA reads round16(len) tokens
             __nv_bfloat16 hh[8], mm[8], ll[8];
+            const float4 f0 = *reinterpret_cast<const float4 *>(sFold + c8 * 8);
+            const float4 f1 = *reinterpret_cast<const float4 *>(sFold + c8 * 8 + 4);
+            const float fs[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int s = c8 * 8 + j;
-                const float w = s < len ? __expf((gh - sGh[s]) + (gl - sGl[s])) * u[s] : 0.f;
-                split3(w, hh[j], mm[j], ll[j]);
-            }
+            for (int j = 0; j < 8; ++j) split3(fs[j] * u[c8 * 8 + j], hh[j], mm[j], ll[j]);
             const uint32_t off = sw128(tid, c8);
             *reinterpret_cast<uint4 *>(sU + off) =
                 make_uint4(pack2(hh[0], hh[1]), pack2(hh[2], hh[3]), pack2(hh[4], hh[5]), pack2(hh[6], hh[7]));
@@ -1164,14 +1168,21 @@ verify4_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs
 //                 after the first MMAs: U~ as three bf16 tiles [64K, 112K), K^T bf16
 //                 [112K, 128K) and the coefficient matrix [128K, 160K)
 //   [160K, 192K)  K, bf16, 2 sub-tiles of 128 rows x 128 B (rows >= C unused)
-//   then: 2 mbarriers, TMEM slot, flag, G (hi, lo), beta, gamma per token.
-__host__ __device__ inline int flush_smem_bytes(int cap) { return 1024 + 196608 + 64 + 16 * round16(cap); }
+//   then: 2 mbarriers, TMEM slot, flag, item count, G (hi, lo), beta, gamma and the
+//   fold factors per token, and the list of sequences to flush (kFlushList entries).
+constexpr int kFlushList = 1024;
+__host__ __device__ inline int flush_smem_bytes(int cap) {
+    return 1024 + 196608 + 64 + 20 * round16(cap) + 4 * kFlushList;
+}
 
+// Persistent: one CTA per SM.  Every CTA lists the sequences that flush (len >=
+// threshold, or len > 0 when forced) and takes (sequence, head) items with a grid
+// stride, so only units with work occupy an SM.
 template <int CMAX>
 __global__ void __launch_bounds__(kThreads, 1)
 flush_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
 {
-    const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int H = a.H, cap = a.cap;
 
     extern __shared__ uint8_t smem_raw[];
@@ -1186,27 +1197,18 @@ flush_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + 16);
     int *flag = reinterpret_cast<int *>(sm + 20);
+    int *n_list = reinterpret_cast<int *>(sm + 24);
     const int GS = round16(cap);                                   // per-token array stride (16-B rows)
     float *sGh = reinterpret_cast<float *>(sm + 64);
     float *sGl = sGh + GS;
     float *sBeta = sGl + GS;
     float *sGam = sBeta + GS;
+    float *sFold = sGam + GS;
+    int *list = reinterpret_cast<int *>(sFold + GS);
 
-    pdl_wait();
-    pdl_release();
-    const int slot = a.state_idx ? a.state_idx[b] : b;
-    if (slot < 0 || slot >= a.n_slot) return;                      // reported by the length kernel
-    const int len = a.buf_len[slot];
-    if (len < 0 || len > cap) return;                               // reported by the length kernel
-    if (!(len >= a.threshold || (a.force && len > 0))) return;
-    const int C = len;
-    const int CP = round16(C);
-    const int LDA = CP + 4;
-
-    if (tid == 0) {
+    if (tid == 0) {                                                 // prologue: no global memory
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
-        *flag = 0;
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
@@ -1214,7 +1216,46 @@ flush_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();
+    pdl_release();
 
+    uint32_t it = 0;                                                // items done by this CTA
+    int *warp_cnt = n_list + 1;                                     // [4] per-warp counts
+    for (int b0 = 0; b0 < a.B; b0 += kFlushList) {
+        // the list must be identical in every CTA: compact in sequence order with
+        // ballots and a prefix over the four warps (no atomics)
+        if (tid == 0) *n_list = 0;
+        __syncthreads();
+        const int bend = min(b0 + kFlushList, a.B);
+        for (int g0 = b0; g0 < bend; g0 += kThreads) {
+            const int bb = g0 + tid;
+            bool f = false;
+            if (bb < bend) {
+                const int sl = a.state_idx ? a.state_idx[bb] : bb;
+                if (sl >= 0 && sl < a.n_slot) {                     // others: reported by the length kernel
+                    const int ln = a.buf_len[sl];
+                    f = ln >= 0 && ln <= cap && (ln >= a.threshold || (a.force && ln > 0));
+                }
+            }
+            const unsigned m = __ballot_sync(0xffffffffu, f);
+            if ((tid & 31) == 0) warp_cnt[warp] = __popc(m);
+            __syncthreads();
+            int base = *n_list;
+            for (int w2 = 0; w2 < warp; ++w2) base += warp_cnt[w2];
+            if (f) list[base + __popc(m & ((1u << (tid & 31)) - 1u))] = bb;
+            __syncthreads();
+            if (tid == 0) *n_list += warp_cnt[0] + warp_cnt[1] + warp_cnt[2] + warp_cnt[3];
+            __syncthreads();
+        }
+        const int n_items = *n_list * H;
+        for (int w = blockIdx.x; w < n_items; w += gridDim.x, ++it) {
+    const int b = list[w / H], h = w % H;
+    const int slot = a.state_idx ? a.state_idx[b] : b;
+    const int len = a.buf_len[slot];
+    const int C = len;
+    const int CP = round16(C);
+    const int LDA = CP + 4;
+    if (tid == 0) *flag = 0;
     const size_t unit = static_cast<size_t>(slot) * H + h;
     const int y = static_cast<int>(unit) * 128;
     if (tid == 0) {
@@ -1233,10 +1274,13 @@ flush_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a
         const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
         if (r < C) raw[i] = __ldg(reinterpret_cast<const uint4 *>(bk + static_cast<size_t>(r) * 128) + c);
     }
-    unsigned short vraw[CMAX];                                      // clamped, unconditional loads
+    constexpr int NVV = CMAX * 16 / kThreads;                       // value rows as 16-byte vectors
+    uint4 vload[NVV];
 #pragma unroll
-    for (int t = 0; t < CMAX; ++t)
-        vraw[t] = __ldg(reinterpret_cast<const unsigned short *>(bv + static_cast<size_t>(t < C ? t : C - 1) * 128) + tid);
+    for (int i = 0; i < NVV; ++i) {
+        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+        if (r < C) vload[i] = __ldg(reinterpret_cast<const uint4 *>(bv + static_cast<size_t>(r) * 128) + c);
+    }
     float gq[2] = {0.f, 0.f}, bq[2] = {0.f, 0.f};
     if (warp == 0) {
 #pragma unroll
@@ -1288,11 +1332,11 @@ flush_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a
             }
         }
     }
-    if (tid == 0 && !mbar_wait(&bar[0], 0)) *flag = 1;
+    if (tid == 0 && !mbar_wait(&bar[0], it & 1)) *flag = 1;
     __syncthreads();
     if (*flag) {
         if (tid == 0) {
-            mbar_wait(&bar[0], 0);
+            mbar_wait(&bar[0], it & 1);
             atomicOr(a.status, kStatusTimeout);
         }
         tc_fence_before();
@@ -1354,6 +1398,12 @@ flush_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a
     }
     tc_fence_after();
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    __nv_bfloat16 *sV = reinterpret_cast<__nv_bfloat16 *>(sX);      // [C][128] in the dead S0 splits
+#pragma unroll
+    for (int i = 0; i < NVV; ++i) {
+        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+        if (r < C) reinterpret_cast<uint4 *>(sV + static_cast<size_t>(r) * 128)[c] = vload[i];
+    }
     // ---- coefficient rows A[t][s] = beta_t e^{G_t-G_s} (k_t.k_s), s < t
     for (int c0 = 0; c0 < CP; c0 += 16) {
         float kq[16];
@@ -1379,6 +1429,10 @@ flush_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a
             for (int j = 0; j < 4; ++j) dst[j] = make_float4(m[4 * j], m[4 * j + 1], m[4 * j + 2], m[4 * j + 3]);
         }
     }
+    if (warp == 0) {                                              // fold factors, shared by all rows
+        const float gh = sGh[C - 1], gl = sGl[C - 1];
+        for (int t = tid; t < CP; t += 32) sFold[t] = t < C ? __expf((gh - sGh[t]) + (gl - sGl[t])) : 0.f;
+    }
     __syncthreads();
     // ---- forward substitution for state row `tid`
     float u[CMAX];
@@ -1399,22 +1453,22 @@ flush_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a
             c2 = fmaf(a4.z, u[s + 2], c2);
             c3 = fmaf(a4.w, u[s + 3], c3);
         }
-        const float vt = __bfloat162float(__ushort_as_bfloat16(vraw[t]));
+        const float vt = __bfloat162float(sV[static_cast<size_t>(t) * 128 + tid]);
         u[t] = sBeta[t] * (vt - sGam[t] * pc[t & 15]) - ((c0 + c1) + (c2 + c3));
     }
     // ---- U~ = e^{G_C - G_s} u_s as three bf16 tiles (row tid, K = token), and K^T
+    __syncthreads();                                                // value rows fully read
     {
-        const float gh = sGh[C - 1], gl = sGl[C - 1];
 #pragma unroll
         for (int c8 = 0; c8 < CMAX / 8; ++c8) {
+            if (c8 * 8 >= CP) break;
             __nv_bfloat16 hh[8], mm[8], ll[8];
+            const float4 f0 = *reinterpret_cast<const float4 *>(sFold + c8 * 8);
+            const float4 f1 = *reinterpret_cast<const float4 *>(sFold + c8 * 8 + 4);
+            const float fs[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int s = c8 * 8 + j;
-                const float w = s < C ? __expf((gh - sGh[s]) + (gl - sGl[s])) * u[s] : 0.f;
-                split3(w, hh[j], mm[j], ll[j]);
-            }
-            if (c8 * 8 < CP) {
+            for (int j = 0; j < 8; ++j) split3(fs[j] * u[c8 * 8 + j], hh[j], mm[j], ll[j]);
+            {
                 const uint32_t off = sw128(tid, c8);
                 *reinterpret_cast<uint4 *>(sU + off) =
                     make_uint4(pack2(hh[0], hh[1]), pack2(hh[2], hh[3]), pack2(hh[4], hh[5]), pack2(hh[6], hh[7]));
@@ -1493,6 +1547,11 @@ flush_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a
         for (int kb = 0; kb < 4; ++kb) tma_store_2d(&tm_state, kb * 32, y, sS + kb * 16384);
         tma_store_commit_and_wait();
     }
+    __syncthreads();                                                // tiles are reused by the next item
+        }
+        __syncthreads();                                            // the list is rebuilt
+    }
+    tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
@@ -1601,8 +1660,11 @@ int tc_flush(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s) {
     auto kern = d->cap <= 48 ? flush_tc_kernel<48> : flush_tc_kernel<64>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return GDN_ERR_LAUNCH;
-    return launch_pdl(kern, dim3(d->H, d->B), dim3(kThreads), smem, s, m, a) == cudaSuccess ? GDN_OK
-                                                                                       : GDN_ERR_LAUNCH;
+    int ctas = resident_ctas(reinterpret_cast<const void *>(kern), smem);
+    if (ctas <= 0) return GDN_ERR_LAUNCH;
+    ctas = ctas < d->B * d->H ? ctas : d->B * d->H;
+    return launch_pdl(kern, dim3(ctas), dim3(kThreads), smem, s, m, a) == cudaSuccess ? GDN_OK
+                                                                                 : GDN_ERR_LAUNCH;
 }
 
 }  // namespace gdn

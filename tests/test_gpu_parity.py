@@ -289,3 +289,30 @@ def test_fused_then_three_call_interleave():
             pr.gpu.flush(force=False)
             pr.orc.flush(force=False)
             pr.step(s)
+
+
+def test_flush_many_sequences_list_chunks():
+    """More sequences than the flush kernel lists at once (1024) and many
+    (sequence, head) items per CTA: every flushed unit is folded exactly once."""
+    import dataclasses
+    import speculative_decode_recurrent_gb300 as lib
+    from harness import gpu_dims, oracle_dims
+    wl = dataclasses.replace(WL["b8"], name="b1100", B=1100, H=2)
+    init = synth.initial_layer(wl, 0)
+    init["buf_len"] = torch.where(init["buf_len"] > 0, torch.full_like(init["buf_len"], wl.threshold),
+                                  init["buf_len"])            # every used slot flushes
+    gd = gpu_dims(wl)
+    gpu = lib.ReplayLayer(gd, init)
+    gpu.flush(force=False)
+    torch.cuda.synchronize()
+    assert int(gpu.status.item()) == 0
+    used = init["state_idx"].long()
+    assert (gpu.t["buf_len"][used] == 0).all()
+    sample = np.array([0, 5, 511, 1023, 1024, 1099])
+    sub = dict(init)
+    sub["state_idx"] = init["state_idx"][sample]
+    od = oracle_dims(wl, B=len(sample), n_slot=gd.n_slot)
+    orc = oracle.Layer(od, sub)
+    orc.flush(force=False)
+    slots = init["state_idx"][sample].long().numpy()
+    assert_close("state", to_np(gpu.t["state"])[slots], orc.state[slots])
