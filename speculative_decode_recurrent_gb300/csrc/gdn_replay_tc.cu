@@ -174,6 +174,103 @@ __device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
     return static_cast<uint32_t>(__bfloat16_as_ushort(a)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
 }
 
+// ---------------------------------------------------------------------------
+// Forward substitution in blocks of 16 tokens (one state row per thread).
+//   u_t = beta_t (v_t - gamma_t P_t) - sum_{s<t} A[t][s] u_s,   t < C
+// and, when Mt is given, the draft sums o[t2] = sum_s M[t2][s] u_s.
+// Earlier blocks' u live in shared memory (this thread's column of sU), so the
+// cross-block update is a rolled loop and the unrolled code is one 16 x 16
+// triangle: the instruction stream stays small enough to be cached.
+//   At  [>= CP rows][LDT]  A transposed (At[s][t] = A[t][s]); zeros at s >= t
+//   Mt  [>= CP rows][16]   M transposed (Mt[s][t2] = M[t2][s]); zeros past p
+//   sV  [C][128] bf16      value rows;  sU [C][128] fp32 receives u
+//   P   TMEM columns [0, C) of this thread's lane (S0 k_t)
+// Tokens t >= C get u = 0 (their coefficient entries may be unset).
+__device__ __forceinline__ void blocked_solve(int C, int tid, uint32_t lane_base, const float *At, int LDT,
+                                              const float *Mt, const __nv_bfloat16 *sV, float *sU,
+                                              const float *sBeta, const float *sGam, float (&o)[16])
+{
+#pragma unroll
+    for (int j = 0; j < 16; ++j) o[j] = 0.f;
+    const int nb = (C + 15) >> 4;
+#pragma unroll 1
+    for (int kb = 0; kb < nb; ++kb) {
+        const int t0 = kb * 16;
+        float pc[16], r[16];
+        tmem_ld16(lane_base + t0, pc);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int t = t0 + j;
+            const float vt = t < C ? __bfloat162float(sV[static_cast<size_t>(t) * 128 + tid]) : 0.f;
+            r[j] = t < C ? sBeta[t] * (vt - sGam[t] * pc[j]) : 0.f;
+        }
+        // contributions of the earlier blocks
+#pragma unroll 2
+        for (int s = 0; s < t0; ++s) {
+            const float us = sU[static_cast<size_t>(s) * 128 + tid];
+            const float4 *a4 = reinterpret_cast<const float4 *>(At + static_cast<size_t>(s) * LDT + t0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 x = a4[q];
+                r[4 * q] = fmaf(-x.x, us, r[4 * q]);
+                r[4 * q + 1] = fmaf(-x.y, us, r[4 * q + 1]);
+                r[4 * q + 2] = fmaf(-x.z, us, r[4 * q + 2]);
+                r[4 * q + 3] = fmaf(-x.w, us, r[4 * q + 3]);
+            }
+        }
+        // the 16 x 16 triangle of this block, right-looking
+#pragma unroll
+        for (int jp = 0; jp < 16; ++jp) {
+            const float uj = (t0 + jp < C) ? r[jp] : 0.f;
+            r[jp] = uj;
+            const float4 *a4 = reinterpret_cast<const float4 *>(At + static_cast<size_t>(t0 + jp) * LDT + t0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 x = a4[q];
+                if (4 * q > jp) r[4 * q] = fmaf(-x.x, uj, r[4 * q]);
+                if (4 * q + 1 > jp) r[4 * q + 1] = fmaf(-x.y, uj, r[4 * q + 1]);
+                if (4 * q + 2 > jp) r[4 * q + 2] = fmaf(-x.z, uj, r[4 * q + 2]);
+                if (4 * q + 3 > jp) r[4 * q + 3] = fmaf(-x.w, uj, r[4 * q + 3]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (t0 + j < C) sU[static_cast<size_t>(t0 + j) * 128 + tid] = r[j];
+        if (Mt) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float4 *m4 = reinterpret_cast<const float4 *>(Mt + static_cast<size_t>(t0 + j) * 16);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 x = m4[q];
+                    o[4 * q] = fmaf(x.x, r[j], o[4 * q]);
+                    o[4 * q + 1] = fmaf(x.y, r[j], o[4 * q + 1]);
+                    o[4 * q + 2] = fmaf(x.z, r[j], o[4 * q + 2]);
+                    o[4 * q + 3] = fmaf(x.w, r[j], o[4 * q + 3]);
+                }
+            }
+        }
+    }
+}
+
+// P[i][C + t2] for t2 < 16 from two 16-column TMEM chunks starting at C & ~15: the
+// uniform rotation by C & 15 keeps every register index static.
+__device__ __forceinline__ void pq_rotate(float (&pq)[2][16], int sh, float (&out)[16]) {
+    float p[32];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) { p[i] = pq[0][i]; p[16 + i] = pq[1][i]; }
+#pragma unroll
+    for (int bit = 0; bit < 4; ++bit) {
+        const int k = 1 << bit;
+        if (sh & k) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) p[i] = i + k < 32 ? p[i + k] : 0.f;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) out[i] = p[i];
+}
+
 // Shared-memory plan of the verify kernel (bytes from the 1024-aligned base):
 //   [0, 64K)          S0 tile (fp32, 4 sub-tiles of 128 rows x 128 B, TMA).  After the
 //                     MMAs, in a folding unit: U~ as three bf16 tiles [0, 48K) and K^T
@@ -259,10 +356,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     const int C = len + T;                   // replayed tokens: buffer, then draft
     const int NP = round16(C + T);           // rows of the [K;Q] operand
     const int CP = round16(C);               // key columns of the K.K / Q.K product
-    const int LDA = CP + 4;
     const int row0 = fold ? 0 : len;         // buffer slot of draft token 0
-    float *sMat = reinterpret_cast<float *>(sB);                  // reused after the MMAs
-    float *sPQ = sMat + static_cast<size_t>(C + T) * LDA;         // [T][128]
 
     const size_t unit = static_cast<size_t>(slot) * H + h;
     const int ytile = static_cast<int>(unit) * 128;
@@ -566,64 +660,54 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
             sFold[t] = t < len ? __expf((gh - sGh[t]) + (gl - sGl[t])) : 0.f;
     }
     __syncthreads();                                              // [K;Q] tile no longer read
+    // value rows sit in sA [0, 16K); the transposed coefficient matrices go to
+    // sA [16K, 36K) (K^T of a fold stays at sA [48K, 64K)) and u to the [K;Q] tile
+    float *Mt = reinterpret_cast<float *>(sA + 16384);            // [CP][16]
+    float *At = reinterpret_cast<float *>(sA + 20480);            // [CP][CP]
+    float *sUf = reinterpret_cast<float *>(sB);                   // [C][128]
     if (tid < C + T) {
+        float *dst = tid < C ? At + tid : Mt + (tid - C);
+        const int ld = tid < C ? CP : 16;
 #pragma unroll
         for (int cb = 0; cb < CMAX / 16; ++cb) {
             if (cb * 16 >= CP) break;
-            float4 *dst = reinterpret_cast<float4 *>(sMat + static_cast<size_t>(tid) * LDA + cb * 16);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                dst[j] = make_float4(m[cb][4 * j], m[cb][4 * j + 1], m[cb][4 * j + 2], m[cb][4 * j + 3]);
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int t = (C & ~15) + 16 * i + j;
-            if (t >= C && t < C + T) sPQ[static_cast<size_t>(t - C) * 128 + tid] = pq[i][j];
+            for (int j = 0; j < 16; ++j) dst[static_cast<size_t>(cb * 16 + j) * ld] = m[cb][j];
         }
     }
     __syncthreads();
 
-    // ---- forward substitution, one state row per thread:
-    //   u_t = beta_t (v_t - gamma_t (S0 k_t)) - sum_{s<t} A[t][s] u_s
-    // Coefficient rows hold zeros at s >= t and u[s] is zero until assigned, so whole
-    // 4-wide groups need no guards.
-    float u[CMAX];
-    float pc[16];
+    // ---- forward substitution and draft sums, then o_t = scale (gamma_p S0 q_t + sum_s M[t][s] u_s)
+    float o[16];
+    blocked_solve(C, tid, lane_base, At, CP, Mt, sV, sUf, sBeta, sGam, o);
+    {
+        float pqr[16];
+        pq_rotate(pq, C & 15, pqr);
 #pragma unroll
-    for (int t = 0; t < CMAX; ++t) u[t] = 0.f;
-#pragma unroll
-    for (int t = 0; t < CMAX; ++t) {
-        if (t >= C) break;
-        if ((t & 15) == 0) tmem_ld16(lane_base + t, pc);
-        const float *Ar = sMat + static_cast<size_t>(t) * LDA;
-        float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
-#pragma unroll
-        for (int s = 0; s < t; s += 4) {
-            const float4 a4 = *reinterpret_cast<const float4 *>(Ar + s);
-            c0 = fmaf(a4.x, u[s], c0);
-            c1 = fmaf(a4.y, u[s + 1], c1);
-            c2 = fmaf(a4.z, u[s + 2], c2);
-            c3 = fmaf(a4.w, u[s + 3], c3);
+        for (int t2 = 0; t2 < 16; ++t2) {
+            if (t2 < T) {
+                const int p = len + t2;
+                a.out[((static_cast<size_t>(b) * T + t2) * H + h) * 128 + tid] =
+                    a.scale * (sGam[p] * pqr[t2] + o[t2]);
+            }
         }
-        const float vt = __bfloat162float(sV[static_cast<size_t>(t) * 128 + tid]);
-        u[t] = sBeta[t] * (vt - sGam[t] * pc[t & 15]) - ((c0 + c1) + (c2 + c3));
     }
     // ---- fold: U~_s = e^{G_{len-1} - G_s} u_s (s < len) as three bf16 tiles, then
-    //      D = U~^T K on the tensor cores while the outputs below run on the ALUs
+    //      D = U~^T K on the tensor cores
     if (fold) {
-        __syncthreads();                                          // value rows (in sA) fully read
-#pragma unroll
-        for (int c8 = 0; c8 < CMAX / 8; ++c8) {
-            if (c8 * 8 >= round16(len)) break;                   // the MMA reads round16(len) tokens
+        __syncthreads();                                          // value rows, coefficients read
+#pragma unroll 1
+        for (int c8 = 0; c8 < round16(len) / 8; ++c8) {          // the MMA reads round16(len) tokens
             __nv_bfloat16 hh[8], mm[8], ll[8];
             const float4 f0 = *reinterpret_cast<const float4 *>(sFold + c8 * 8);
             const float4 f1 = *reinterpret_cast<const float4 *>(sFold + c8 * 8 + 4);
             const float fs[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
 #pragma unroll
-            for (int j = 0; j < 8; ++j) split3(fs[j] * u[c8 * 8 + j], hh[j], mm[j], ll[j]);
+            for (int j = 0; j < 8; ++j) {
+                const int t = c8 * 8 + j;
+                const float ut = t < len ? sUf[static_cast<size_t>(t) * 128 + tid] : 0.f;
+                split3(fs[j] * ut, hh[j], mm[j], ll[j]);
+            }
             const uint32_t off = sw128(tid, c8);
             *reinterpret_cast<uint4 *>(sU + off) =
                 make_uint4(pack2(hh[0], hh[1]), pack2(hh[2], hh[3]), pack2(hh[4], hh[5]), pack2(hh[6], hh[7]));
@@ -646,24 +730,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
                              (sp | ks) != 0);
             mma_commit(&bar[3]);
         }
-    }
-    // ---- draft outputs o_t = scale (gamma_p S0 q_t + sum_{s<=p} e^{G_p-G_s} (q_t.k_s) u_s);
-    // the coefficient rows are zero past p, so each sum stops at the 16-block holding p
-    for (int t2 = 0; t2 < T; ++t2) {
-        const int p = len + t2;
-        const float *Mr = sMat + static_cast<size_t>(C + t2) * LDA;
-        float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
-#pragma unroll
-        for (int s = 0; s < CMAX; s += 4) {
-            if ((s & 15) == 0 && s > p) break;
-            const float4 m4 = *reinterpret_cast<const float4 *>(Mr + s);
-            c0 = fmaf(m4.x, u[s], c0);
-            c1 = fmaf(m4.y, u[s + 1], c1);
-            c2 = fmaf(m4.z, u[s + 2], c2);
-            c3 = fmaf(m4.w, u[s + 3], c3);
-        }
-        const float o = sGam[p] * sPQ[static_cast<size_t>(t2) * 128 + tid] + ((c0 + c1) + (c2 + c3));
-        a.out[((static_cast<size_t>(b) * T + t2) * H + h) * 128 + tid] = a.scale * o;
     }
     if (fold) {
         // ---- new checkpoint S_len = gamma_{len-1} S0 + D, written over the S0 tile and
@@ -727,14 +793,15 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
 //   [SB, SB + 32K)   S0, one K-half at a time (TMA): 2 sub-tiles of 128 rows x 128 B.
 //                    An M = 128 operand starting in the [K;Q] tile reads on into this
 //                    tile; those rows feed accumulator lanes that are never read.
-//   after both halves the same bytes hold the value rows (bf16, [C][128]), the
-//   coefficient matrices (row stride CP + 4) and the S0 q columns ([T][128])
+//   after both halves the same bytes hold the value rows (bf16, [C][128]), u ([C][128])
+//   and the coefficient matrices transposed (A^T [CP][CP], M^T [CP][16])
 //   then: 4 mbarriers, TMEM slot, flag, G (hi, lo), beta, gamma per token.
 constexpr int kTmemCols4 = 128;
 __host__ __device__ inline int v4_sb_bytes(int cap, int T) { return 2 * round16(cap + T) * 128; }
 __host__ __device__ inline int v4_region_bytes(int cap, int T) {
     const int tiles = v4_sb_bytes(cap, T) + 32768;
-    const int need = cap * 256 + (cap + T) * (round16(cap) + 4) * 4 + T * 512;
+    const int cp = round16(cap);
+    const int need = cap * 768 + cp * cp * 4 + cp * 64;       // values, u, A^T, M^T
     return tiles > need ? tiles : ((need + 1023) & ~1023);
 }
 __host__ __device__ inline int v4_smem_bytes(int cap, int T) { return v4_region_bytes(cap, T) + 64 + 16 * round16(cap); }
@@ -800,7 +867,6 @@ verify4_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs
     const int C = len + T;
     const int NP = round16(C + T);
     const int CP = round16(C);
-    const int LDA = CP + 4;
 
     const size_t unit = static_cast<size_t>(slot) * H + h;
     const int ytile = static_cast<int>(unit) * 128;
@@ -1089,72 +1155,38 @@ verify4_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs
         const int c0 = (C & ~15) + 16 * i;
         if (c0 < C + T) tmem_ld16(lane_base + c0, pq[i]);
     }
-    // the tiles are free: value rows, coefficient rows and S0 q columns take their place
+    // the tiles are free: value rows, u, and the coefficient matrices (transposed) take
+    // their place
     __nv_bfloat16 *sV = reinterpret_cast<__nv_bfloat16 *>(smem_raw);          // [C][128]
-    float *sMat = reinterpret_cast<float *>(smem_raw + static_cast<size_t>(C) * 256);
-    float *sPQ = sMat + static_cast<size_t>(C + T) * LDA;                     // [T][128]
+    float *sU = reinterpret_cast<float *>(smem_raw + static_cast<size_t>(C) * 256);   // [C][128]
+    float *At = sU + static_cast<size_t>(C) * 128;                           // [CP][CP]
+    float *Mt = At + static_cast<size_t>(CP) * CP;                            // [CP][16]
 #pragma unroll
     for (int i = 0; i < NVV; ++i) {
         const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
         if (r < C) reinterpret_cast<uint4 *>(sV + static_cast<size_t>(r) * 128)[c] = vload[i];
     }
     if (tid < C + T) {
+        float *dst = tid < C ? At + tid : Mt + (tid - C);
+        const int ld = tid < C ? CP : 16;
 #pragma unroll
         for (int cb = 0; cb < CMAX / 16; ++cb) {
             if (cb * 16 >= CP) break;
-            float4 *dst = reinterpret_cast<float4 *>(sMat + static_cast<size_t>(tid) * LDA + cb * 16);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                dst[j] = make_float4(m[cb][4 * j], m[cb][4 * j + 1], m[cb][4 * j + 2], m[cb][4 * j + 3]);
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int t = (C & ~15) + 16 * i + j;
-            if (t >= C && t < C + T) sPQ[static_cast<size_t>(t - C) * 128 + tid] = pq[i][j];
+            for (int j = 0; j < 16; ++j) dst[static_cast<size_t>(cb * 16 + j) * ld] = m[cb][j];
         }
     }
     __syncthreads();
-    // ---- forward substitution, one state row per thread (see the two-CTA kernel)
-    float u[CMAX];
-    float pc[16];
+    float o[16];
+    blocked_solve(C, tid, lane_base, At, CP, Mt, sV, sU, sBeta, sGam, o);
+    float pqr[16];
+    pq_rotate(pq, C & 15, pqr);
 #pragma unroll
-    for (int t = 0; t < CMAX; ++t) u[t] = 0.f;
-#pragma unroll
-    for (int t = 0; t < CMAX; ++t) {
-        if (t >= C) break;
-        if ((t & 15) == 0) tmem_ld16(lane_base + t, pc);
-        const float *Ar = sMat + static_cast<size_t>(t) * LDA;
-        float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
-#pragma unroll
-        for (int s = 0; s < t; s += 4) {
-            const float4 a4 = *reinterpret_cast<const float4 *>(Ar + s);
-            c0 = fmaf(a4.x, u[s], c0);
-            c1 = fmaf(a4.y, u[s + 1], c1);
-            c2 = fmaf(a4.z, u[s + 2], c2);
-            c3 = fmaf(a4.w, u[s + 3], c3);
+    for (int t2 = 0; t2 < 16; ++t2) {
+        if (t2 < T) {
+            const int p = len + t2;
+            a.out[((static_cast<size_t>(b) * T + t2) * H + h) * 128 + tid] = a.scale * (sGam[p] * pqr[t2] + o[t2]);
         }
-        const float vt = __bfloat162float(sV[static_cast<size_t>(t) * 128 + tid]);
-        u[t] = sBeta[t] * (vt - sGam[t] * pc[t & 15]) - ((c0 + c1) + (c2 + c3));
-    }
-    // ---- draft outputs
-    for (int t2 = 0; t2 < T; ++t2) {
-        const int p = len + t2;
-        const float *Mr = sMat + static_cast<size_t>(C + t2) * LDA;
-        float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
-#pragma unroll
-        for (int s = 0; s < CMAX; s += 4) {
-            if ((s & 15) == 0 && s > p) break;
-            const float4 m4 = *reinterpret_cast<const float4 *>(Mr + s);
-            c0 = fmaf(m4.x, u[s], c0);
-            c1 = fmaf(m4.y, u[s + 1], c1);
-            c2 = fmaf(m4.z, u[s + 2], c2);
-            c3 = fmaf(m4.w, u[s + 3], c3);
-        }
-        const float o = sGam[p] * sPQ[static_cast<size_t>(t2) * 128 + tid] + ((c0 + c1) + (c2 + c3));
-        a.out[((static_cast<size_t>(b) * T + t2) * H + h) * 128 + tid] = a.scale * o;
     }
     tc_fence_before();
     __syncthreads();
@@ -1254,7 +1286,6 @@ flush_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a
     const int len = a.buf_len[slot];
     const int C = len;
     const int CP = round16(C);
-    const int LDA = CP + 4;
     if (tid == 0) *flag = 0;
     const size_t unit = static_cast<size_t>(slot) * H + h;
     const int y = static_cast<int>(unit) * 128;
@@ -1404,7 +1435,25 @@ flush_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a
         const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
         if (r < C) reinterpret_cast<uint4 *>(sV + static_cast<size_t>(r) * 128)[c] = vload[i];
     }
-    // ---- coefficient rows A[t][s] = beta_t e^{G_t-G_s} (k_t.k_s), s < t
+    // ---- K^T row `tid` (key channel j = tid): k_s[j] for s < CP, zero past C; built
+    //      before the key tile is reused for u
+    {
+        const __nv_bfloat16 zero = __float2bfloat16_rn(0.f);
+        for (int c8 = 0; c8 < CP / 8; ++c8) {
+            __nv_bfloat16 kk[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int s2 = c8 * 8 + j;
+                kk[j] = s2 < C ? *reinterpret_cast<const __nv_bfloat16 *>(
+                                     sK + (tid >> 6) * 16384 + sw128(s2, (tid & 63) >> 3) + (tid & 7) * 2)
+                               : zero;
+            }
+            *reinterpret_cast<uint4 *>(sKt + sw128(tid, c8)) =
+                make_uint4(pack2(kk[0], kk[1]), pack2(kk[2], kk[3]), pack2(kk[4], kk[5]), pack2(kk[6], kk[7]));
+        }
+    }
+    // ---- coefficient rows A[t][s] = beta_t e^{G_t-G_s} (k_t.k_s), s < t, stored transposed
+    float *At = sMat;                                               // [CP][CP]
     for (int c0 = 0; c0 < CP; c0 += 16) {
         float kq[16];
         tmem_ld16(lane_base + CP + c0, kq);
@@ -1418,80 +1467,45 @@ flush_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a
                 gs[4 * j] = x.x; gs[4 * j + 1] = x.y; gs[4 * j + 2] = x.z; gs[4 * j + 3] = x.w;
                 ls[4 * j] = y.x; ls[4 * j + 1] = y.y; ls[4 * j + 2] = y.z; ls[4 * j + 3] = y.w;
             }
-            float m[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const float e = __expf((gh - gs[j]) + (gl - ls[j]));
-                m[j] = (c0 + j < tid) ? be * e * kq[j] : 0.f;
+                At[static_cast<size_t>(c0 + j) * CP + tid] = (c0 + j < tid) ? be * e * kq[j] : 0.f;
             }
-            float4 *dst = reinterpret_cast<float4 *>(sMat + static_cast<size_t>(tid) * LDA + c0);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = make_float4(m[4 * j], m[4 * j + 1], m[4 * j + 2], m[4 * j + 3]);
         }
     }
     if (warp == 0) {                                              // fold factors, shared by all rows
         const float gh = sGh[C - 1], gl = sGl[C - 1];
         for (int t = tid; t < CP; t += 32) sFold[t] = t < C ? __expf((gh - sGh[t]) + (gl - sGl[t])) : 0.f;
     }
-    __syncthreads();
-    // ---- forward substitution for state row `tid`
-    float u[CMAX];
-    float pc[16];
-#pragma unroll
-    for (int t = 0; t < CMAX; ++t) u[t] = 0.f;
-#pragma unroll
-    for (int t = 0; t < CMAX; ++t) {
-        if (t >= C) break;
-        if ((t & 15) == 0) tmem_ld16(lane_base + t, pc);
-        const float *Ar = sMat + static_cast<size_t>(t) * LDA;
-        float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
-#pragma unroll
-        for (int s = 0; s < t; s += 4) {                            // zeros at s >= t (see verify)
-            const float4 a4 = *reinterpret_cast<const float4 *>(Ar + s);
-            c0 = fmaf(a4.x, u[s], c0);
-            c1 = fmaf(a4.y, u[s + 1], c1);
-            c2 = fmaf(a4.z, u[s + 2], c2);
-            c3 = fmaf(a4.w, u[s + 3], c3);
-        }
-        const float vt = __bfloat162float(sV[static_cast<size_t>(t) * 128 + tid]);
-        u[t] = sBeta[t] * (vt - sGam[t] * pc[t & 15]) - ((c0 + c1) + (c2 + c3));
-    }
-    // ---- U~ = e^{G_C - G_s} u_s as three bf16 tiles (row tid, K = token), and K^T
-    __syncthreads();                                                // value rows fully read
+    __syncthreads();                                                // key tile read, coefficients in place
+    // ---- forward substitution (u into the key tile's bytes), then U~ = e^{G_C - G_s} u_s
+    //      as three bf16 tiles (row tid, K = token)
+    float *sUf = reinterpret_cast<float *>(sK);                     // [C][128]
     {
+        float unused[16];
+        blocked_solve(C, tid, lane_base, At, CP, nullptr, sV, sUf, sBeta, sGam, unused);
+    }
+    __syncthreads();                                                // value rows fully read
+#pragma unroll 1
+    for (int c8 = 0; c8 < CP / 8; ++c8) {
+        __nv_bfloat16 hh[8], mm[8], ll[8];
+        const float4 f0 = *reinterpret_cast<const float4 *>(sFold + c8 * 8);
+        const float4 f1 = *reinterpret_cast<const float4 *>(sFold + c8 * 8 + 4);
+        const float fs[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
 #pragma unroll
-        for (int c8 = 0; c8 < CMAX / 8; ++c8) {
-            if (c8 * 8 >= CP) break;
-            __nv_bfloat16 hh[8], mm[8], ll[8];
-            const float4 f0 = *reinterpret_cast<const float4 *>(sFold + c8 * 8);
-            const float4 f1 = *reinterpret_cast<const float4 *>(sFold + c8 * 8 + 4);
-            const float fs[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
-#pragma unroll
-            for (int j = 0; j < 8; ++j) split3(fs[j] * u[c8 * 8 + j], hh[j], mm[j], ll[j]);
-            {
-                const uint32_t off = sw128(tid, c8);
-                *reinterpret_cast<uint4 *>(sU + off) =
-                    make_uint4(pack2(hh[0], hh[1]), pack2(hh[2], hh[3]), pack2(hh[4], hh[5]), pack2(hh[6], hh[7]));
-                *reinterpret_cast<uint4 *>(sU + 16384 + off) =
-                    make_uint4(pack2(mm[0], mm[1]), pack2(mm[2], mm[3]), pack2(mm[4], mm[5]), pack2(mm[6], mm[7]));
-                *reinterpret_cast<uint4 *>(sU + 32768 + off) =
-                    make_uint4(pack2(ll[0], ll[1]), pack2(ll[2], ll[3]), pack2(ll[4], ll[5]), pack2(ll[6], ll[7]));
-            }
+        for (int j = 0; j < 8; ++j) {
+            const int t = c8 * 8 + j;
+            const float ut = t < C ? sUf[static_cast<size_t>(t) * 128 + tid] : 0.f;
+            split3(fs[j] * ut, hh[j], mm[j], ll[j]);
         }
-        // K^T row `tid` (key channel j = tid): k_s[j] for s < CP, zero past C
-        const __nv_bfloat16 zero = __float2bfloat16_rn(0.f);
-        for (int c8 = 0; c8 < CP / 8; ++c8) {
-            __nv_bfloat16 kk[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int s = c8 * 8 + j;
-                kk[j] = s < C ? *reinterpret_cast<const __nv_bfloat16 *>(
-                                    sK + (tid >> 6) * 16384 + sw128(s, (tid & 63) >> 3) + (tid & 7) * 2)
-                              : zero;
-            }
-            *reinterpret_cast<uint4 *>(sKt + sw128(tid, c8)) =
-                make_uint4(pack2(kk[0], kk[1]), pack2(kk[2], kk[3]), pack2(kk[4], kk[5]), pack2(kk[6], kk[7]));
-        }
+        const uint32_t off = sw128(tid, c8);
+        *reinterpret_cast<uint4 *>(sU + off) =
+            make_uint4(pack2(hh[0], hh[1]), pack2(hh[2], hh[3]), pack2(hh[4], hh[5]), pack2(hh[6], hh[7]));
+        *reinterpret_cast<uint4 *>(sU + 16384 + off) =
+            make_uint4(pack2(mm[0], mm[1]), pack2(mm[2], mm[3]), pack2(mm[4], mm[5]), pack2(mm[6], mm[7]));
+        *reinterpret_cast<uint4 *>(sU + 32768 + off) =
+            make_uint4(pack2(ll[0], ll[1]), pack2(ll[2], ll[3]), pack2(ll[4], ll[5]), pack2(ll[6], ll[7]));
     }
     fence_proxy_async();
     tc_fence_before();
