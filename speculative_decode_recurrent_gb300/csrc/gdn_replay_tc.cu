@@ -170,6 +170,11 @@ __device__ __forceinline__ void split3(float x, __nv_bfloat16 &h, __nv_bfloat16 
     m = __float2bfloat16_rn(r1);
     l = __float2bfloat16_rn(r1 - __bfloat162float(m));
 }
+// Two bf16 terms whose sum is x to a relative 2^-16.
+__device__ __forceinline__ void split2(float x, __nv_bfloat16 &h, __nv_bfloat16 &l) {
+    h = __float2bfloat16_rn(x);
+    l = __float2bfloat16_rn(x - __bfloat162float(h));
+}
 __device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
     return static_cast<uint32_t>(__bfloat16_as_ushort(a)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
 }
@@ -782,35 +787,68 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
 }
 
 // ---------------------------------------------------------------------------
-// Four-CTA verify (no fold; cap <= 48, T <= 16).  Two CTAs per SM leave the SM idle
-// once the first wave's loads are in; with 128 TMEM columns, at most ~50 KB of shared
-// memory and 128 registers per thread, four CTAs fit on an SM and the whole decode
-// batch runs in one wave.  The checkpoint streams through in two K-halves of 64
-// columns (32 KB), each followed by its half of the S0 [K;Q]^T and [K;Q] K^T MMAs.
+// Verify by effective queries (no fold; T <= 16, C = len + T <= CMAX).
 //
-// Shared-memory plan (bytes from the 1024-aligned base):
-//   [0, SB)          [K;Q] fp32, one K-half at a time: 2 sub-tiles of NPmax rows x 128 B
-//   [SB, SB + 32K)   S0, one K-half at a time (TMA): 2 sub-tiles of 128 rows x 128 B.
-//                    An M = 128 operand starting in the [K;Q] tile reads on into this
-//                    tile; those rows feed accumulator lanes that are never read.
-//   after both halves the same bytes hold the value rows (bf16, [C][128]), u ([C][128])
-//   and the coefficient matrices transposed (A^T [CP][CP], M^T [CP][16])
-//   then: 4 mbarriers, TMEM slot, flag, G (hi, lo), beta, gamma per token.
-constexpr int kTmemCols4 = 128;
-__host__ __device__ inline int v4_sb_bytes(int cap, int T) { return 2 * round16(cap + T) * 128; }
-__host__ __device__ inline int v4_region_bytes(int cap, int T) {
-    const int tiles = v4_sb_bytes(cap, T) + 32768;
-    const int cp = round16(cap);
-    const int need = cap * 768 + cp * cp * 4 + cp * 64;       // values, u, A^T, M^T
-    return tiles > need ? tiles : ((need + 1023) & ~1023);
+// The chunked form gives u = (I + A)^{-1} r with r_s = beta_s (v_s - gamma_s S0 k_s),
+// A[t][s] = beta_t e^{G_t-G_s} (k_t.k_s) (s < t), and the draft outputs
+// o_t2 = scale (gamma_p S0 q_t2 + sum_s M[t2][s] u_s) with
+// M[t2][s] = e^{G_p-G_s} (q_t2.k_s) (s <= p = len + t2).  With W = M (I + A)^{-1}
+// (T x C) the sum is sum_s W[t2][s] r_s, so
+//   o_t2 = scale (S0 qe_t2 + ve_t2),
+//   qe_t2 = gamma_p q_t2 - sum_s W[t2][s] beta_s gamma_s k_s,
+//   ve_t2 = sum_s W[t2][s] beta_s v_s.
+// The checkpoint enters a single M = 128, N = 16 contraction; everything else
+// depends on the tokens only.  W comes from the back substitution
+// W[t2][s] = M[t2][s] - sum_{s' > s} W[t2][s'] A[s'][s], one warp per four draft
+// rows and one lane per two token columns; qe and ve are bf16 contractions of the
+// key and value rows (read as MN-major operands, no transpose) with W beta gamma
+// and W beta split into two bf16 terms each (relative error 2^-16).
+// The checkpoint is prefetched into L2 at the start and streamed through two
+// 16 KB buffers in quarters of 32 columns once the token work is done.
+//
+// Shared-memory plan (bytes from the 1024-aligned base), NPA = round16(CMAX + 16):
+//   [0, 2 SUBK)          [K;Q] rows, bf16, 2 sub-tiles (d_k halves) of NPA rows x 128 B
+//   [OFF_V, +2 SUBV)     value rows, bf16, 2 sub-tiles of CMAX rows x 128 B
+//   [OFF_A, +CMAX^2 4)   A, fp32, row-major [CMAX][CMAX]
+//   [OFF_M, +16 CMAX 4)  M, fp32, row-major [16][CMAX]
+//   [OFF_W, +8K)         W beta gamma and W beta as 2 + 2 bf16 tiles [16][64]; later
+//                        qe as fp32 [16][128] (4 sub-tiles of 16 rows x 128 B)
+//   [0, 32K)             after the token contractions: two checkpoint quarter buffers
+//   [OFF_S, ...)         8 mbarriers, TMEM slot, flag, then G (hi, lo), beta, gamma
+// An M = 128 operand starting in the [K;Q] tile reads on past its NPA rows; those
+// rows only feed accumulator lanes that are never read.
+constexpr int kTmemColsEq = 128;
+template <int CMAX> struct EqPlan {
+    static constexpr int NPA = (CMAX + 16 + 15) & ~15;
+    static constexpr int SUBK = NPA * 128;
+    static constexpr int SUBV = CMAX * 128;
+    static constexpr int OFF_V = 2 * SUBK;
+    static constexpr int OFF_A = OFF_V + 2 * SUBV;
+    static constexpr int OFF_M = OFF_A + CMAX * CMAX * 4;
+    static constexpr int OFF_W = (OFF_M + 16 * CMAX * 4 + 1023) & ~1023;
+    static constexpr int OFF_S = OFF_W + 8192;
+    static constexpr int BYTES = OFF_S + 128 + 16 * CMAX;
+    static_assert(OFF_W >= 32768, "the quarter buffers must not reach the qe tile");
+    static_assert(SUBK + 16384 <= BYTES, "M = 128 operand reads stay inside the allocation");
+    static_assert(CMAX % 16 == 0 && CMAX <= 64, "token columns: at most two per lane");
+    static_assert((SUBK % 1024) == 0 && (OFF_V % 1024) == 0 && (SUBV % 1024) == 0, "swizzle atoms");
+};
+
+// MN-major operand, 128-byte swizzle: 64-element atoms along M/N `lbo` bytes apart,
+// 8-row groups along K 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t addr, uint32_t lbo) {
+    return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
 }
-__host__ __device__ inline int v4_smem_bytes(int cap, int T) { return v4_region_bytes(cap, T) + 64 + 16 * round16(cap); }
+constexpr uint32_t kIdescMnMajorA = 1u << 15;
 
 template <int CMAX>
 __global__ void __launch_bounds__(kThreads, 4)
-verify4_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
+verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
 {
-    const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+    using P = EqPlan<CMAX>;
+    const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = a.T, H = a.H, cap = a.cap;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -818,25 +856,30 @@ verify4_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs
         if (tid == 0) atomicOr(a.status, kStatusTimeout);
         return;
     }
-    uint8_t *sB = smem_raw;
-    uint8_t *sA = smem_raw + v4_sb_bytes(cap, T);
-    uint8_t *sm = smem_raw + v4_region_bytes(cap, T);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm);            // TMA (2 phases), MMA half 0, K.K, P
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + 32);
-    int *flag = reinterpret_cast<int *>(sm + 36);
-    const int GS = round16(cap);
-    float *sGh = reinterpret_cast<float *>(sm + 64);
-    float *sGl = sGh + GS;
-    float *sBeta = sGl + GS;
-    float *sGam = sBeta + GS;
+    uint8_t *sKQ = smem_raw;
+    uint8_t *sV = smem_raw + P::OFF_V;
+    float *sAm = reinterpret_cast<float *>(smem_raw + P::OFF_A);
+    float *sMm = reinterpret_cast<float *>(smem_raw + P::OFF_M);
+    uint8_t *sW = smem_raw + P::OFF_W;
+    uint8_t *sQe = sW;
+    uint8_t *sm = smem_raw + P::OFF_S;
+    // 0, 1: checkpoint buffers (TMA); 2: K.K; 3: qe, ve; 4..7: checkpoint quarter MMAs
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + 64);
+    int *flag = reinterpret_cast<int *>(sm + 68);
+    float *sGh = reinterpret_cast<float *>(sm + 128);
+    float *sGl = sGh + CMAX;
+    float *sBeta = sGl + CMAX;
+    float *sGam = sBeta + CMAX;
+    constexpr int COL_Q = CMAX, COL_V = CMAX + 16, COL_O = CMAX + 32;   // TMEM columns
 
     if (tid == 0) {                                               // prologue: no global memory
 #pragma unroll
-        for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
+        for (int i = 0; i < 8; ++i) mbar_init(&bar[i], 1);
         *flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0) tmem_alloc(tmem_slot, kTmemCols4);
+    if (warp == 0) tmem_alloc(tmem_slot, kTmemColsEq);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -857,51 +900,24 @@ verify4_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs
     else if (!other_class && (len < 0 || len + T > cap))
         bad = len < 0 || len > cap ? GDN_STATUS_BAD_LEN : GDN_STATUS_NO_ROOM;
     pdl_release();                                                // every length of this CTA is read
+    auto finish = [&]() {
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tmem, kTmemColsEq);
+        if (waiter) pdl_wait();
+    };
     if (bad || other_class) {                                     // uniform across the CTA
         if (bad && tid == 0 && h == 0 && !split) atomicOr(a.status, bad);
-        __syncthreads();
-        if (warp == 0) tmem_dealloc(tmem, kTmemCols4);
-        if (waiter) pdl_wait();
+        finish();
         return;
     }
     const int C = len + T;
-    const int NP = round16(C + T);
     const int CP = round16(C);
-
     const size_t unit = static_cast<size_t>(slot) * H + h;
     const int ytile = static_cast<int>(unit) * 128;
-    if (tid == 0) {                                               // S0 columns 0..63; 64..127 into L2
-        mbar_expect_tx(&bar[0], 32768);
-        tma_load_2d(sA, &tm_state, 0, ytile, &bar[0]);
-        tma_load_2d(sA + 16384, &tm_state, 32, ytile, &bar[0]);
-        prefetch_tile_l2(&tm_state, 64, ytile);
-        prefetch_tile_l2(&tm_state, 96, ytile);
-    }
-    if (a.prefetch_stride > 0 && warp == 1) {                     // the unit one wave later -> L2
-        const int lane = tid & 31;
-        const int nxt = b * gridDim.x + h + a.prefetch_stride;
-        if (nxt < static_cast<int>(gridDim.x * gridDim.y)) {
-            const int nb = nxt / gridDim.x, nh = nxt % gridDim.x;
-            const int ns = a.state_idx ? a.state_idx[nb] : nb;
-            if (ns >= 0 && ns < a.n_slot) {
-                const int nlen = min(max(a.buf_len[ns], 0), cap);
-                const size_t nunit = static_cast<size_t>(ns) * H + nh;
-                if (lane < 4) prefetch_tile_l2(&tm_state, lane * 32, static_cast<int>(nunit) * 128);
-                if (lane == 4 && nlen > 0)
-                    prefetch_l2(reinterpret_cast<const __nv_bfloat16 *>(a.buf_k) + nunit * cap * 128, nlen * 256);
-                if (lane == 5 && nlen > 0)
-                    prefetch_l2(reinterpret_cast<const __nv_bfloat16 *>(a.buf_v) + nunit * cap * 128, nlen * 256);
-                const size_t nrow0 = (static_cast<size_t>(nb) * T * H + nh) * 128;
-                for (int r = lane; r < 3 * T; r += 32) {
-                    const void *base3 = r < T ? a.k : r < 2 * T ? a.q : a.v;
-                    prefetch_l2(reinterpret_cast<const __nv_bfloat16 *>(base3) + nrow0 +
-                                    static_cast<size_t>(r % T) * H * 128, 256);
-                }
-            }
-        }
-    }
 
-    // ---- every global load of this unit, issued back to back
+    // ---- every global load of this unit, issued back to back (the checkpoint, needed
+    //      last, is prefetched into L2 once these rows are in, so they come first)
     const __nv_bfloat16 *bk = reinterpret_cast<const __nv_bfloat16 *>(a.buf_k) + unit * cap * 128;
     const __nv_bfloat16 *bv = reinterpret_cast<const __nv_bfloat16 *>(a.buf_v) + unit * cap * 128;
     const size_t drow0 = (static_cast<size_t>(b) * T * H + h) * 128;
@@ -911,11 +927,12 @@ verify4_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs
     const __nv_bfloat16 *dv = reinterpret_cast<const __nv_bfloat16 *>(a.v) + drow0;
     __nv_bfloat16 *wk = reinterpret_cast<__nv_bfloat16 *>(a.buf_k) + (unit * cap + len) * 128;
     __nv_bfloat16 *wv = reinterpret_cast<__nv_bfloat16 *>(a.buf_v) + (unit * cap + len) * 128;
-    constexpr int NV = (CMAX + 16) * 16 / kThreads;
+    constexpr int NV = P::NPA * 16 / kThreads;                   // 16-byte vectors of [K;Q] per thread
     uint4 raw[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+        raw[i] = make_uint4(0u, 0u, 0u, 0u);
         if (r < C + T) {
             const __nv_bfloat16 *src = r < len ? bk + static_cast<size_t>(r) * 128
                                      : r < C   ? dk + static_cast<size_t>(r - len) * dstride
@@ -928,6 +945,7 @@ verify4_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs
 #pragma unroll
     for (int i = 0; i < NVV; ++i) {
         const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+        vload[i] = make_uint4(0u, 0u, 0u, 0u);
         if (r < C) {
             const __nv_bfloat16 *src = r < len ? bv + static_cast<size_t>(r) * 128
                                                : dv + static_cast<size_t>(r - len) * dstride;
@@ -938,7 +956,7 @@ verify4_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs
     if (warp == 0) {
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-            const int t = (tid & 31) + 32 * i;
+            const int t = lane + 32 * i;
             if (t < C) {
                 if (t < len) {
                     gq[i] = a.buf_g[unit * cap + t];
@@ -951,30 +969,21 @@ verify4_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs
             }
         }
     }
-    // ---- K-half 0 of [K;Q] (columns 0..63) into the swizzled fp32 tile; draft keys
-    //      and values into the buffer (slots len .. len + T - 1, never read here)
+    // ---- rows into the swizzled bf16 tiles (zeros past the last token); the draft
+    //      keys and values into the buffer (slots len .. len + T - 1, never read here)
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
-        if (r < C + T) {
-            if (r >= len && r < C) reinterpret_cast<uint4 *>(wk + static_cast<size_t>(r - len) * 128)[c] = raw[i];
-            if (c < 8) {
-                float f[8];
-                bf16x8_to_f32(raw[i], f);
-                uint8_t *tile = sB + (c >> 2) * NP * 128;
-                const int ch = (c & 3) * 2;
-                *reinterpret_cast<float4 *>(tile + sw128(r, ch)) = make_float4(f[0], f[1], f[2], f[3]);
-                *reinterpret_cast<float4 *>(tile + sw128(r, ch + 1)) = make_float4(f[4], f[5], f[6], f[7]);
-            }
-        }
+        *reinterpret_cast<uint4 *>(sKQ + (c >> 3) * P::SUBK + sw128(r, c & 7)) = raw[i];
+        if (r >= len && r < C) reinterpret_cast<uint4 *>(wk + static_cast<size_t>(r - len) * 128)[c] = raw[i];
     }
 #pragma unroll
     for (int i = 0; i < NVV; ++i) {
         const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+        *reinterpret_cast<uint4 *>(sV + (c >> 3) * P::SUBV + sw128(r, c & 7)) = vload[i];
         if (r >= len && r < C) reinterpret_cast<uint4 *>(wv + static_cast<size_t>(r - len) * 128)[c] = vload[i];
     }
     if (warp == 0) {                                              // compensated scan of g
-        const int lane = tid & 31;
         float hi[2], lo[2];
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -1000,12 +1009,13 @@ verify4_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int t = lane + 32 * i;
-            if (t < C) {
-                sGh[t] = hi[i];
-                sGl[t] = lo[i];
-                sGam[t] = __expf(hi[i] + lo[i]);
-                sBeta[t] = bq[i];
-                if (t >= len) {
+            if (t < CMAX) {                                       // zeros past the last token
+                const bool live = t < C;
+                sGh[t] = live ? hi[i] : 0.f;
+                sGl[t] = live ? lo[i] : 0.f;
+                sGam[t] = live ? __expf(hi[i] + lo[i]) : 0.f;
+                sBeta[t] = live ? bq[i] : 0.f;
+                if (live && t >= len) {
                     a.buf_g[unit * cap + t] = gq[i];
                     a.buf_beta[unit * cap + t] = bq[i];
                 }
@@ -1014,127 +1024,144 @@ verify4_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs
     }
     fence_proxy_async();
     __syncthreads();
-    const uint32_t idP = idesc_mn(2, 128, NP), idK = idesc_mn(2, 128, CP);
-    const uint32_t a0 = saddr(sA), b0 = saddr(sB);
-    if (tid == 0) {
-        if (mbar_wait(&bar[0], 0)) {
-            tc_fence_after();
+    const uint32_t kq0 = saddr(sKQ), v0 = saddr(sV), w0 = saddr(sW), qe0 = saddr(sQe), s00 = saddr(smem_raw);
+    if (tid == 0) {                                               // [K;Q] K^T: coefficients
+        tc_fence_after();
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {                       // K-half 0: 8 steps of 8 columns
-                const uint32_t off = (ks & 3) * 32;
-                const uint64_t db = desc_sw128(b0 + (ks >> 2) * NP * 128 + off);
-                mma_tf32(tmem + NP, db, db, idK, ks > 0);
-                mma_tf32(tmem, desc_sw128(a0 + (ks >> 2) * 16384 + off), db, idP, ks > 0);
-            }
-            mma_commit(&bar[1]);
-        } else {
-            *flag = 1;
+        for (int q = 0; q < 4; ++q) prefetch_tile_l2(&tm_state, q * 32, ytile);
+        const uint32_t idK = idesc_mn(1, 128, CP);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint64_t d = desc_sw128(kq0 + (ks >> 2) * P::SUBK + (ks & 3) * 32);
+            mma_bf16(tmem, d, d, idK, ks > 0);
         }
+        mma_commit(&bar[2]);
     }
-    __syncthreads();
-    bool ok = *flag == 0;
-    if (ok) ok = mbar_wait(&bar[1], 0);
+    // this thread's query column (d_k = tid) for qe, read before the tiles are reused
+    float qcol[16];
+#pragma unroll
+    for (int t2 = 0; t2 < 16; ++t2) {
+        const int r = C + t2;                                     // < NPA
+        const __nv_bfloat16 x = *reinterpret_cast<const __nv_bfloat16 *>(
+            sKQ + (tid >> 6) * P::SUBK + sw128(r, (tid & 63) >> 3) + (tid & 7) * 2);
+        qcol[t2] = t2 < T ? __bfloat162float(x) : 0.f;
+    }
+    bool ok = mbar_wait(&bar[2], 0);
     if (__syncthreads_or(!ok)) {
         if (tid == 0) {
-            mbar_wait(&bar[0], 0);
-            if (*flag == 0) mbar_wait(&bar[1], 0);
+            mbar_wait(&bar[2], 0);
             atomicOr(a.status, kStatusTimeout);
         }
-        tc_fence_before();
-        __syncthreads();
-        if (warp == 0) tmem_dealloc(tmem, kTmemCols4);
-        if (waiter) pdl_wait();
-        return;
-    }
-    tc_fence_after();
-    // ---- K-half 1: S0 columns 64..127 (L2-warm) and [K;Q] columns 64..127
-    if (tid == 0) {
-        mbar_expect_tx(&bar[0], 32768);
-        tma_load_2d(sA, &tm_state, 64, ytile, &bar[0]);
-        tma_load_2d(sA + 16384, &tm_state, 96, ytile, &bar[0]);
-    }
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
-        if (r < C + T && c >= 8) {
-            float f[8];
-            bf16x8_to_f32(raw[i], f);
-            uint8_t *tile = sB + ((c - 8) >> 2) * NP * 128;
-            const int ch = (c & 3) * 2;
-            *reinterpret_cast<float4 *>(tile + sw128(r, ch)) = make_float4(f[0], f[1], f[2], f[3]);
-            *reinterpret_cast<float4 *>(tile + sw128(r, ch + 1)) = make_float4(f[4], f[5], f[6], f[7]);
-        }
-    }
-    fence_proxy_async();
-    __syncthreads();
-    if (tid == 0) {
-        if (mbar_wait(&bar[0], 1)) {
-            tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t db = desc_sw128(b0 + (ks >> 2) * NP * 128 + (ks & 3) * 32);
-                mma_tf32(tmem + NP, db, db, idK, 1);
-            }
-            mma_commit(&bar[2]);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t off = (ks & 3) * 32;
-                mma_tf32(tmem, desc_sw128(a0 + (ks >> 2) * 16384 + off),
-                         desc_sw128(b0 + (ks >> 2) * NP * 128 + off), idP, 1);
-            }
-            mma_commit(&bar[3]);
-        } else {
-            *flag = 1;
-        }
-    }
-    __syncthreads();
-    ok = *flag == 0;
-    if (ok) ok = mbar_wait(&bar[2], 0);
-    if (__syncthreads_or(!ok)) {
-        if (tid == 0) {
-            mbar_wait(&bar[0], 1);
-            if (*flag == 0) {
-                mbar_wait(&bar[2], 0);
-                mbar_wait(&bar[3], 0);
-            }
-            atomicOr(a.status, kStatusTimeout);
-        }
-        tc_fence_before();
-        __syncthreads();
-        if (warp == 0) tmem_dealloc(tmem, kTmemCols4);
-        if (waiter) pdl_wait();
+        finish();
         return;
     }
     tc_fence_after();
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    // ---- coefficient rows (registers until the P MMA has released the tiles)
-    float m[CMAX / 16][16];
-    {
+    // ---- coefficient rows: TMEM lane r = row r of [K;Q]; key rows t < C give
+    //      A[t][s] = beta_t e^{G_t-G_s} (k_t.k_s) (s < t), query rows C + t2 give
+    //      M[t2][s] = e^{G_p-G_s} (q_t2.k_s) (s <= p); rows t2 >= T of M are zero
+    if (warp * 32 < C + 16) {                                     // warp-uniform: the loads are collective
         const bool is_q = tid >= C;
-        const int p = tid >= C + T ? C - 1 : is_q ? len + (tid - C) : tid;
+        const int t2 = tid - C;
+        const bool writes = tid < C + 16;
+        const bool live = tid < C + T;
+        const int p = !live ? C - 1 : is_q ? len + t2 : tid;
         const float gh = sGh[p], gl = sGl[p];
         const float scl = is_q ? 1.f : sBeta[p];
-        const int lim = tid >= C + T ? 0 : is_q ? min(p + 1, C) : tid;
+        const int lim = !live ? 0 : is_q ? min(p + 1, C) : tid;
+        float *dst = is_q ? sMm + (writes ? t2 : 0) * CMAX : sAm + tid * CMAX;
 #pragma unroll
         for (int cb = 0; cb < CMAX / 16; ++cb) {
             const int c0 = cb * 16;
-            if (c0 >= CP) break;
             float kq[16];
-            tmem_ld16(lane_base + NP + c0, kq);
-            float gs[16], ls[16];
+            if (c0 < CP) {
+                tmem_ld16(lane_base + c0, kq);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float4 x = *reinterpret_cast<const float4 *>(sGh + c0 + 4 * j);
-                const float4 y = *reinterpret_cast<const float4 *>(sGl + c0 + 4 * j);
-                gs[4 * j] = x.x; gs[4 * j + 1] = x.y; gs[4 * j + 2] = x.z; gs[4 * j + 3] = x.w;
-                ls[4 * j] = y.x; ls[4 * j + 1] = y.y; ls[4 * j + 2] = y.z; ls[4 * j + 3] = y.w;
+                for (int j = 0; j < 16; ++j) kq[j] = 0.f;
             }
+            float mrow[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float e = __expf((gh - gs[j]) + (gl - ls[j]));
-                m[cb][j] = (c0 + j < lim) ? scl * e * kq[j] : 0.f;
+            for (int j4 = 0; j4 < 4; ++j4) {
+                const float4 x = *reinterpret_cast<const float4 *>(sGh + c0 + 4 * j4);
+                const float4 y = *reinterpret_cast<const float4 *>(sGl + c0 + 4 * j4);
+                const float gs[4] = {x.x, x.y, x.z, x.w}, ls[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int s = c0 + 4 * j4 + j;
+                    const float e = __expf((gh - gs[j]) + (gl - ls[j]));
+                    mrow[4 * j4 + j] = s < lim ? scl * e * kq[4 * j4 + j] : 0.f;
+                }
+            }
+            if (writes) {
+#pragma unroll
+                for (int j4 = 0; j4 < 4; ++j4)
+                    *reinterpret_cast<float4 *>(dst + c0 + 4 * j4) =
+                        make_float4(mrow[4 * j4], mrow[4 * j4 + 1], mrow[4 * j4 + 2], mrow[4 * j4 + 3]);
             }
         }
+    }
+    __syncthreads();
+    // ---- W = M (I + A)^{-1}: warp w holds draft rows 4w .. 4w + 3, lane l token columns
+    //      l and l + 32; column s is final once every s' > s has been subtracted
+    float x0[4], x1[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float *mr = sMm + (4 * warp + i) * CMAX;
+        x0[i] = mr[lane];
+        x1[i] = lane + 32 < CMAX ? mr[lane + 32] : 0.f;
+    }
+#pragma unroll 2
+    for (int s = C - 1; s >= 0; --s) {
+        const float *ar = sAm + s * CMAX;
+        const float a0 = ar[lane], a1 = lane + 32 < CMAX ? ar[lane + 32] : 0.f;
+        const bool upper = s >= 32;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float w = __shfl_sync(0xffffffffu, upper ? x1[i] : x0[i], s & 31);
+            x0[i] = fmaf(-w, a0, x0[i]);
+            x1[i] = fmaf(-w, a1, x1[i]);
+        }
+    }
+    // ---- W beta gamma and W beta as K-major [16][64] tiles, each the sum of two bf16
+    //      terms (relative error 2^-16, far below that of the tf32 checkpoint product)
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int s = lane + 32 * half;
+        if (s < CMAX) {
+            const float bs = sBeta[s], bg = bs * sGam[s];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int t2 = 4 * warp + i;
+                const float w = half ? x1[i] : x0[i];
+                __nv_bfloat16 t4[4];
+                split2(w * bg, t4[0], t4[1]);
+                split2(w * bs, t4[2], t4[3]);
+                const uint32_t off = sw128(t2, s >> 3) + (s & 7) * 2;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) *reinterpret_cast<__nv_bfloat16 *>(sW + j * 2048 + off) = t4[j];
+            }
+        }
+    }
+    fence_proxy_async();
+    __syncthreads();
+    if (tid == 0) {                                               // qe^T and ve^T, M = 128, N = 16
+        tc_fence_after();
+        const uint32_t idQ = idesc_mn(1, 128, 16) | kIdescMnMajorA;
+        const int nks = CP / 16;
+#pragma unroll
+        for (int ks = 0; ks < CMAX / 16; ++ks) {
+            if (ks < nks) {
+                const uint64_t ak = desc_mn_sw128(kq0 + ks * 2048, P::SUBK);
+                const uint64_t av = desc_mn_sw128(v0 + ks * 2048, P::SUBV);
+#pragma unroll
+                for (int sp = 0; sp < 2; ++sp) {
+                    mma_bf16(tmem + COL_Q, ak, desc_sw128(w0 + sp * 2048 + ks * 32), idQ, (sp | ks) != 0);
+                    mma_bf16(tmem + COL_V, av, desc_sw128(w0 + (2 + sp) * 2048 + ks * 32), idQ, (sp | ks) != 0);
+                }
+            }
+        }
+        mma_commit(&bar[3]);
     }
     ok = mbar_wait(&bar[3], 0);
     if (__syncthreads_or(!ok)) {
@@ -1142,56 +1169,82 @@ verify4_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs
             mbar_wait(&bar[3], 0);
             atomicOr(a.status, kStatusTimeout);
         }
-        tc_fence_before();
-        __syncthreads();
-        if (warp == 0) tmem_dealloc(tmem, kTmemCols4);
-        if (waiter) pdl_wait();
+        finish();
         return;
     }
     tc_fence_after();
-    float pq[2][16];
+    // the token tiles are free: the first two checkpoint quarters come in from L2
+    if (tid == 0) {
+        fence_proxy_async();
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int c0 = (C & ~15) + 16 * i;
-        if (c0 < C + T) tmem_ld16(lane_base + c0, pq[i]);
+        for (int q = 0; q < 2; ++q) {
+            mbar_expect_tx(&bar[q], 16384);
+            tma_load_2d(smem_raw + q * 16384, &tm_state, q * 32, ytile, &bar[q]);
+        }
     }
-    // the tiles are free: value rows, u, and the coefficient matrices (transposed) take
-    // their place
-    __nv_bfloat16 *sV = reinterpret_cast<__nv_bfloat16 *>(smem_raw);          // [C][128]
-    float *sU = reinterpret_cast<float *>(smem_raw + static_cast<size_t>(C) * 256);   // [C][128]
-    float *At = sU + static_cast<size_t>(C) * 128;                           // [CP][CP]
-    float *Mt = At + static_cast<size_t>(CP) * CP;                            // [CP][16]
+    {                                                             // qe[t2][d_k = tid], fp32 K-major tile
+        float dq[16];
+        tmem_ld16(lane_base + COL_Q, dq);
+        uint8_t *col = sQe + (tid >> 5) * 2048 + (tid & 3) * 4;
 #pragma unroll
-    for (int i = 0; i < NVV; ++i) {
-        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
-        if (r < C) reinterpret_cast<uint4 *>(sV + static_cast<size_t>(r) * 128)[c] = vload[i];
+        for (int t2 = 0; t2 < 16; ++t2) {
+            const float ge = t2 < T ? sGam[len + t2] : 0.f;
+            *reinterpret_cast<float *>(col + sw128(t2, (tid & 31) >> 2)) = fmaf(ge, qcol[t2], -dq[t2]);
+        }
     }
-    if (tid < C + T) {
-        float *dst = tid < C ? At + tid : Mt + (tid - C);
-        const int ld = tid < C ? CP : 16;
+    fence_proxy_async();
+    __syncthreads();
+    if (tid == 0) {                                               // O = S0 qe^T, quarter by quarter
+        tc_fence_after();
+        const uint32_t idO = idesc_mn(2, 128, 16);
+        int loads[2] = {1, 1};                                    // TMA loads issued per buffer
+        int mmas = 0;                                             // quarters whose MMAs were issued
+        bool good = true;
+        for (int q = 0; q < 4; ++q) {
+            const int buf = q & 1;
+            if (!mbar_wait(&bar[buf], q >> 1)) { good = false; break; }
+            tc_fence_after();
 #pragma unroll
-        for (int cb = 0; cb < CMAX / 16; ++cb) {
-            if (cb * 16 >= CP) break;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) dst[static_cast<size_t>(cb * 16 + j) * ld] = m[cb][j];
+            for (int ks = 0; ks < 4; ++ks)
+                mma_tf32(tmem + COL_O, desc_sw128(s00 + buf * 16384 + ks * 32),
+                         desc_sw128(qe0 + q * 2048 + ks * 32), idO, (q | ks) != 0);
+            mma_commit(&bar[4 + q]);
+            mmas = q + 1;
+            if (q < 2) {                                          // the buffer is reused once its MMAs are done
+                if (!mbar_wait(&bar[4 + q], 0)) { good = false; break; }
+                mbar_expect_tx(&bar[buf], 16384);
+                tma_load_2d(smem_raw + buf * 16384, &tm_state, (q + 2) * 32, ytile, &bar[buf]);
+                ++loads[buf];
+            }
+        }
+        if (!good) {                                              // wait (bounded) for what is in flight
+            for (int q = 0; q < mmas; ++q) mbar_wait(&bar[4 + q], 0);
+            for (int i = 0; i < 2; ++i) mbar_wait(&bar[i], (loads[i] - 1) & 1);
+            *flag = 1;
         }
     }
     __syncthreads();
-    float o[16];
-    blocked_solve(C, tid, lane_base, At, CP, Mt, sV, sU, sBeta, sGam, o);
-    float pqr[16];
-    pq_rotate(pq, C & 15, pqr);
-#pragma unroll
-    for (int t2 = 0; t2 < 16; ++t2) {
-        if (t2 < T) {
-            const int p = len + t2;
-            a.out[((static_cast<size_t>(b) * T + t2) * H + h) * 128 + tid] = a.scale * (sGam[p] * pqr[t2] + o[t2]);
+    ok = *flag == 0;
+    if (ok) ok = mbar_wait(&bar[7], 0);
+    if (__syncthreads_or(!ok)) {
+        if (tid == 0) {
+            if (*flag == 0) mbar_wait(&bar[7], 0);
+            atomicOr(a.status, kStatusTimeout);
         }
+        finish();
+        return;
     }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kTmemCols4);
-    if (waiter) pdl_wait();
+    tc_fence_after();
+    {
+        float o[16], ve[16];
+        tmem_ld16(lane_base + COL_O, o);
+        tmem_ld16(lane_base + COL_V, ve);
+#pragma unroll
+        for (int t2 = 0; t2 < 16; ++t2)
+            if (t2 < T)
+                a.out[((static_cast<size_t>(b) * T + t2) * H + h) * 128 + tid] = a.scale * (o[t2] + ve[t2]);
+    }
+    finish();
 }
 
 // Shared-memory plan of the flush kernel (bytes from the 1024-aligned base):
@@ -1608,15 +1661,12 @@ int resident_ctas(const void *kern, int smem) {
     return sms * per_sm;
 }
 
-int launch_verify4(const gdn_replay_dims *d, const ReplayArgs &a0, const CUtensorMap &m, cudaStream_t s) {
-    const int smem = v4_smem_bytes(d->cap, d->T);
-    auto kern = verify4_tc_kernel<48>;
-    static int stride = -1;
+template <int CMAX>
+int launch_eq(const gdn_replay_dims *d, const ReplayArgs &a, const CUtensorMap &m, cudaStream_t s) {
+    constexpr int smem = EqPlan<CMAX>::BYTES;
+    auto kern = verify_eq_kernel<CMAX>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return GDN_ERR_LAUNCH;
-    if (stride < 0) stride = resident_ctas(reinterpret_cast<const void *>(kern), smem);
-    ReplayArgs a = a0;
-    a.prefetch_stride = stride;
     return launch_pdl(kern, dim3(d->H, d->B), dim3(kThreads), smem, s, m, a) == cudaSuccess ? GDN_OK
                                                                                        : GDN_ERR_LAUNCH;
 }
@@ -1644,9 +1694,8 @@ int tc_verify(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s, boo
     if (verify_smem_bytes(cmax, d->T) > 227 * 1024) return 1;
     CUtensorMap m;
     if (!state_map(&m, a.state_in, d->n_slot * d->H * 128)) return 1;
-    if (!fold && d->cap <= 48) return launch_verify4(d, a, m, s);
-    if (fold) return cmax <= 48 ? launch_verify<48, true>(d, a, m, s) : launch_verify<64, true>(d, a, m, s);
-    return cmax <= 48 ? launch_verify<48, false>(d, a, m, s) : launch_verify<64, false>(d, a, m, s);
+    if (!fold) return cmax <= 48 ? launch_eq<48>(d, a, m, s) : launch_eq<64>(d, a, m, s);
+    return cmax <= 48 ? launch_verify<48, true>(d, a, m, s) : launch_verify<64, true>(d, a, m, s);
 }
 
 int tc_verify_fold_split(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s) {
@@ -1662,7 +1711,7 @@ int tc_verify_fold_split(const gdn_replay_dims *d, const ReplayArgs &a, cudaStre
     if (rc) return rc;
     ReplayArgs an = a;
     an.fold_class = 1;                                            // the rest, beside the fold launch
-    return launch_verify4(d, an, m, s);
+    return launch_eq<48>(d, an, m, s);
 }
 
 int tc_flush(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s) {
