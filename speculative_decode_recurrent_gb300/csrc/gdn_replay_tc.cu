@@ -884,21 +884,22 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // fold_class 1: this launch runs beside the fold launch that precedes it and must
-    // not wait for it (every CTA of that launch has waited for the earlier kernels
-    // before letting this one start); CTA (0, 0) waits for it at the end instead, so
-    // the following kernel still observes both launches as complete.
+    // fold_class 1: the units that do not fold, in a launch that runs beside the fold
+    // launch preceding it and must not wait for it (every CTA of that launch has
+    // waited for the earlier kernels before letting this one start); CTA (0, 0) waits
+    // for it at the end instead, so the next kernel observes both launches complete.
+    // It reports the length errors of every sequence (the fold launch skips them).
     const bool split = a.fold_class == 1;
     const bool waiter = split && blockIdx.x == 0 && blockIdx.y == 0;
     if (!split) pdl_wait();
 
     const int slot = a.state_idx ? a.state_idx[b] : b;
     const int len = (slot >= 0 && slot < a.n_slot) ? a.buf_len[slot] : 0;
-    int bad = 0;
     const bool other_class = split && len >= a.threshold && len <= cap;   // the fold launch's unit
+    int bad = 0;
     if (slot < 0 || slot >= a.n_slot) bad = GDN_STATUS_BAD_SLOT;
-    else if (!other_class && (len < 0 || len + T > cap))
-        bad = len < 0 || len > cap ? GDN_STATUS_BAD_LEN : GDN_STATUS_NO_ROOM;
+    else if (len < 0 || len > cap) bad = GDN_STATUS_BAD_LEN;
+    else if (!other_class && len + T > cap) bad = GDN_STATUS_NO_ROOM;
     pdl_release();                                                // every length of this CTA is read
     auto finish = [&]() {
         tc_fence_before();
@@ -907,7 +908,7 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
         if (waiter) pdl_wait();
     };
     if (bad || other_class) {                                     // uniform across the CTA
-        if (bad && tid == 0 && h == 0 && !split) atomicOr(a.status, bad);
+        if (bad && tid == 0 && h == 0) atomicOr(a.status, bad);
         finish();
         return;
     }
@@ -1623,6 +1624,695 @@ flush_tc_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
+// ---------------------------------------------------------------------------
+// Fold (flush) through the inverse of the token system.
+//
+// For the L buffered tokens of one (sequence, head), with D_s = e^{G_{L-1}-G_s} and
+// Tinv = (I + A)^{-1}, the checkpoint after the buffer is
+//   S_L = gamma_{L-1} S0 + sum_s D_s u_s k_s^T,  u = Tinv r,  r_s = beta_s (v_s - gamma_s S0 k_s),
+// and exchanging the sums gives S_L = gamma_{L-1} S0 + R E with the columns r_s in
+// R (d_v x L) and E[s'] = sum_s Tinv[s][s'] D_s k_s (L x d_k).  E depends on the tokens
+// only, so the triangular work happens on an L x L matrix, not per state row:
+//   1. [K] K^T on the tensor cores (bf16 rows as loaded), A in shared memory;
+//   2. Tinv by blocks of 16: the diagonal blocks by forward substitution (a thread
+//      per column), the blocks below by T_ij = -T_ii sum_k A_ik T_kj, one block
+//      diagonal at a time;
+//   3. E^T = K^T F^T with F[s'][s] = D_s Tinv[s][s'] split into two bf16 terms, the
+//      keys read as an MN-major operand;
+//   4. with the checkpoint (TMA from L2, quarters of 32 columns through two 16 KB
+//      buffers): S0 K^T in tf32, R in registers, R and E^T each as two bf16 terms,
+//      and one M = 128, N = 128 contraction (hi.hi + hi.lo + lo.hi, relative error
+//      about 2^-16, far below that of the tf32 S0 K^T).
+// Persistent: the CTAs list the sequences that flush (len >= threshold, or len > 0
+// when forced) in the same order and take (sequence, head) items with a grid stride.
+//
+// Shared-memory plan (bytes from the 1024-aligned base), Lp = CMAX:
+//   [0, 2 SUBK)            key rows, bf16, 2 sub-tiles of CMAX rows x 128 B
+//   [OFF_AT, +Lp^2 4)      A^T, fp32 (row s holds column s of A)
+//   [OFF_TI, +Lp^2 4)      Tinv, fp32 row-major
+//   [0, 32K)               after E^T is formed: E^T as two bf16 tiles [128][64]
+//   [OFF_V, +2 SUBV)       value rows, bf16
+//   [OFF_KF, +4 KFSUB)     key rows, fp32, 4 sub-tiles of CMAX rows x 128 B (S0 K^T)
+//   [OFF_Q, +32K)          F as two bf16 tiles [CMAX][64] and the block scratch; then
+//                          the two checkpoint buffers; then R as two bf16 tiles [128][64]
+//   [0, 64K)               after the fold contraction: the new state, for the TMA store
+//   [OFF_SC, ...)          mbarriers, TMEM slot, flags, G (hi, lo), beta, gamma, D, list
+template <int CMAX> struct FoldPlan {
+    static constexpr int SUBK = CMAX * 128;
+    static constexpr int OFF_AT = 2 * SUBK;
+    static constexpr int OFF_TI = OFF_AT + CMAX * CMAX * 4;
+    static constexpr int OFF_V = 32768 > OFF_TI + CMAX * CMAX * 4 ? 32768 : ((OFF_TI + CMAX * CMAX * 4 + 1023) & ~1023);
+    static constexpr int SUBV = CMAX * 128;
+    static constexpr int OFF_KF = OFF_V + 2 * SUBV;
+    static constexpr int KFSUB = CMAX * 128;
+    static constexpr int OFF_Q = OFF_KF + 4 * KFSUB;
+    static constexpr int OFF_Y = OFF_Q + 2 * CMAX * 128;      // Tinv block scratch (phase A)
+    static constexpr int OFF_SC = OFF_Q + 32768;
+    static constexpr int LIST = 512;
+    static constexpr int BYTES = OFF_SC + 128 + 20 * CMAX + 4 * LIST + 256;
+    static_assert(CMAX == 48 || CMAX == 64, "token blocks");
+    static_assert(SUBK + 16384 <= OFF_SC, "M = 128 operand reads stay inside the allocation");
+    static_assert(OFF_Y + 3 * 1024 <= OFF_SC, "block scratch");
+    static_assert(OFF_V >= 32768 && OFF_V + 2 * SUBV + 4 * KFSUB <= OFF_Q, "E^T tiles below the values");
+    static_assert(OFF_SC >= 65536, "staging of the new state");
+    static_assert((OFF_V % 1024) == 0 && (OFF_KF % 1024) == 0 && (OFF_Q % 1024) == 0 && (SUBK % 1024) == 0 &&
+                  (KFSUB % 1024) == 0, "swizzle atoms");
+};
+
+template <int CMAX, bool DRAFT>
+__global__ void __launch_bounds__(kThreads, 2)
+fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
+{
+    using P = FoldPlan<CMAX>;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = a.H, cap = a.cap;
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if (saddr(smem_raw) & 1023u) {
+        if (tid == 0) atomicOr(a.status, kStatusTimeout);
+        return;
+    }
+    uint8_t *sK = smem_raw;
+    float *sAt = reinterpret_cast<float *>(smem_raw + P::OFF_AT);
+    float *sTi = reinterpret_cast<float *>(smem_raw + P::OFF_TI);
+    uint8_t *sEt = smem_raw;                                      // 2 x 16 KB
+    uint8_t *sV = smem_raw + P::OFF_V;
+    uint8_t *sKf = smem_raw + P::OFF_KF;
+    uint8_t *sF = smem_raw + P::OFF_Q;                            // 2 x CMAX x 128 B
+    float *sY = reinterpret_cast<float *>(smem_raw + P::OFF_Y);   // [3][16][16]
+    uint8_t *sBuf = smem_raw + P::OFF_Q;                          // 2 x 16 KB
+    uint8_t *sR = smem_raw + P::OFF_Q;                            // 2 x 16 KB
+    uint8_t *sNew = smem_raw;                                     // 64 KB
+    uint8_t *sm = smem_raw + P::OFF_SC;
+    // 0: K.K; 1: E^T; 2, 3: checkpoint buffers; 4..7: S0 K^T quarters; 8: fold; 9: draft
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + 80);
+    int *flag = reinterpret_cast<int *>(sm + 84);
+    int *n_list = reinterpret_cast<int *>(sm + 88);
+    int *warp_cnt = reinterpret_cast<int *>(sm + 96);              // [4]
+    float *sGh = reinterpret_cast<float *>(sm + 128);
+    float *sGl = sGh + CMAX;
+    float *sBeta = sGl + CMAX;
+    float *sGam = sBeta + CMAX;
+    float *sD = sGam + CMAX;
+    int *list = reinterpret_cast<int *>(sD + CMAX);
+    float *dGh = reinterpret_cast<float *>(list + P::LIST);      // draft: G (hi, lo), beta, gamma
+    float *dGl = dGh + 16;
+    float *dBeta = dGl + 16;
+    float *dGam = dBeta + 16;
+    constexpr uint32_t COL_KK = 0, COL_E = 64, COL_P = 0, COL_F = 128;
+
+    if (tid == 0) {
+#pragma unroll
+        for (int i = 0; i < 10; ++i) mbar_init(&bar[i], 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    pdl_wait();
+    pdl_release();
+    const uint32_t k0 = saddr(sK), f0 = saddr(sF), kf0 = saddr(sKf), buf0 = saddr(sBuf), r0 = saddr(sR),
+                   e0 = saddr(sEt);
+
+    uint32_t it = 0;                                              // items done by this CTA
+    bool alive = true;
+    for (int b0 = 0; b0 < a.B && alive; b0 += P::LIST) {
+        // the list must be identical in every CTA: compact in sequence order with
+        // ballots and a prefix over the four warps (no atomics)
+        if (tid == 0) *n_list = 0;
+        __syncthreads();
+        const int bend = min(b0 + P::LIST, a.B);
+        for (int g0 = b0; g0 < bend; g0 += kThreads) {
+            const int bb = g0 + tid;
+            bool f = false;
+            if (bb < bend) {
+                const int sl = a.state_idx ? a.state_idx[bb] : bb;
+                if (sl >= 0 && sl < a.n_slot) {                     // others: reported by the length kernel
+                    const int ln = a.buf_len[sl];
+                    f = ln >= 0 && ln <= cap && (ln >= a.threshold || (a.force && ln > 0));
+                }
+            }
+            const unsigned m = __ballot_sync(0xffffffffu, f);
+            if (lane == 0) warp_cnt[warp] = __popc(m);
+            __syncthreads();
+            int base = *n_list;
+            for (int w2 = 0; w2 < warp; ++w2) base += warp_cnt[w2];
+            if (f) list[base + __popc(m & ((1u << lane) - 1u))] = bb;
+            __syncthreads();
+            if (tid == 0) *n_list += warp_cnt[0] + warp_cnt[1] + warp_cnt[2] + warp_cnt[3];
+            __syncthreads();
+        }
+        const int n_items = *n_list * H;
+        for (int w = blockIdx.x; w < n_items && alive; w += gridDim.x, ++it) {
+            const uint32_t ph = it & 1u;
+            const int b = list[w / H], h = w % H;
+            const int slot = a.state_idx ? a.state_idx[b] : b;
+            const int L = a.buf_len[slot];
+            const int Lp = round16(L);
+            const int nb = Lp >> 4;
+            const size_t unit = static_cast<size_t>(slot) * H + h;
+            const int ytile = static_cast<int>(unit) * 128;
+            if (tid == 0) {
+                *flag = 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) prefetch_tile_l2(&tm_state, q * 32, ytile);
+            }
+            // ---- token rows: keys (bf16 tile, fp32 tile), values (bf16 tile), gates
+            const __nv_bfloat16 *bk = reinterpret_cast<const __nv_bfloat16 *>(a.buf_k) + unit * cap * 128;
+            const __nv_bfloat16 *bv = reinterpret_cast<const __nv_bfloat16 *>(a.buf_v) + unit * cap * 128;
+            constexpr int NV = CMAX * 16 / kThreads;
+            uint4 raw[NV], vload[NV];
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+                raw[i] = make_uint4(0u, 0u, 0u, 0u);
+                vload[i] = make_uint4(0u, 0u, 0u, 0u);
+                if (r < L) {
+                    raw[i] = __ldg(reinterpret_cast<const uint4 *>(bk + static_cast<size_t>(r) * 128) + c);
+                    vload[i] = __ldg(reinterpret_cast<const uint4 *>(bv + static_cast<size_t>(r) * 128) + c);
+                }
+            }
+            float gq[2] = {0.f, 0.f}, bq[2] = {0.f, 0.f};
+            if (warp == 0) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int t = lane + 32 * i;
+                    if (t < L) {
+                        gq[i] = a.buf_g[unit * cap + t];
+                        bq[i] = a.buf_beta[unit * cap + t];
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+                *reinterpret_cast<uint4 *>(sK + (c >> 3) * P::SUBK + sw128(r, c & 7)) = raw[i];
+                *reinterpret_cast<uint4 *>(sV + (c >> 3) * P::SUBV + sw128(r, c & 7)) = vload[i];
+                float fl[8];
+                bf16x8_to_f32(raw[i], fl);
+                uint8_t *tile = sKf + (c >> 2) * P::KFSUB;
+                const int ch = (c & 3) * 2;
+                *reinterpret_cast<float4 *>(tile + sw128(r, ch)) = make_float4(fl[0], fl[1], fl[2], fl[3]);
+                *reinterpret_cast<float4 *>(tile + sw128(r, ch + 1)) = make_float4(fl[4], fl[5], fl[6], fl[7]);
+            }
+            if (warp == 0) {                                      // compensated scan of g
+                float hi[2], lo[2];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    hi[i] = gq[i];
+                    lo[i] = 0.f;
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const float h2 = __shfl_up_sync(0xffffffffu, hi[i], off);
+                        const float l2 = __shfl_up_sync(0xffffffffu, lo[i], off);
+                        if (lane >= off) {
+                            const float s1 = hi[i] + h2, bp = s1 - hi[i];
+                            lo[i] += l2 + ((hi[i] - (s1 - bp)) + (h2 - bp));
+                            hi[i] = s1;
+                        }
+                    }
+                }
+                const float chh = __shfl_sync(0xffffffffu, hi[0], 31), cll = __shfl_sync(0xffffffffu, lo[0], 31);
+                {
+                    const float s1 = hi[1] + chh, bp = s1 - hi[1];
+                    lo[1] += cll + ((hi[1] - (s1 - bp)) + (chh - bp));
+                    hi[1] = s1;
+                }
+                // G_{L-1} (hi, lo) from the lane that holds it
+                const int src = (L - 1) & 31;
+                const float gLh = __shfl_sync(0xffffffffu, (L - 1) >= 32 ? hi[1] : hi[0], src);
+                const float gLl = __shfl_sync(0xffffffffu, (L - 1) >= 32 ? lo[1] : lo[0], src);
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int t = lane + 32 * i;
+                    if (t < CMAX) {
+                        const bool live = t < L;
+                        sGh[t] = live ? hi[i] : 0.f;
+                        sGl[t] = live ? lo[i] : 0.f;
+                        sGam[t] = live ? __expf(hi[i] + lo[i]) : 0.f;
+                        sBeta[t] = live ? bq[i] : 0.f;
+                        sD[t] = live ? __expf((gLh - hi[i]) + (gLl - lo[i])) : 0.f;
+                    }
+                }
+            }
+            fence_proxy_async();
+            __syncthreads();
+            if (tid == 0) {                                       // K K^T
+                tc_fence_after();
+                const uint32_t idK = idesc_mn(1, 128, Lp);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t d = desc_sw128(k0 + (ks >> 2) * P::SUBK + (ks & 3) * 32);
+                    mma_bf16(tmem + COL_KK, d, d, idK, ks > 0);
+                }
+                mma_commit(&bar[0]);
+            }
+            bool ok = mbar_wait(&bar[0], ph);
+            if (__syncthreads_or(!ok)) {
+                if (tid == 0) { mbar_wait(&bar[0], ph); atomicOr(a.status, kStatusTimeout); }
+                alive = false;
+                break;
+            }
+            tc_fence_after();
+            // ---- A^T: thread t writes column t of A (row t of A^T): A[t][s] for s < t
+            if (warp * 32 < CMAX) {                               // warp-uniform: collective loads
+                const int t = tid;
+                const float gh = t < L ? sGh[t] : 0.f, gl = t < L ? sGl[t] : 0.f, bt = t < L ? sBeta[t] : 0.f;
+#pragma unroll
+                for (int cb = 0; cb < CMAX / 16; ++cb) {
+                    const int c0 = cb * 16;
+                    float kk[16];
+                    if (c0 < Lp) {
+                        tmem_ld16(lane_base + COL_KK + c0, kk);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) kk[j] = 0.f;
+                    }
+                    float gs[16], ls[16], av[16];
+#pragma unroll
+                    for (int j4 = 0; j4 < 4; ++j4) {
+                        const float4 x = *reinterpret_cast<const float4 *>(sGh + c0 + 4 * j4);
+                        const float4 y = *reinterpret_cast<const float4 *>(sGl + c0 + 4 * j4);
+                        gs[4 * j4] = x.x; gs[4 * j4 + 1] = x.y; gs[4 * j4 + 2] = x.z; gs[4 * j4 + 3] = x.w;
+                        ls[4 * j4] = y.x; ls[4 * j4 + 1] = y.y; ls[4 * j4 + 2] = y.z; ls[4 * j4 + 3] = y.w;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int s = c0 + j;
+                        const float e = __expf((gh - gs[j]) + (gl - ls[j]));
+                        av[j] = (s < t && t < L) ? bt * e * kk[j] : 0.f;
+                    }
+                    if (t < CMAX) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) sAt[(c0 + j) * CMAX + t] = av[j];
+                    }
+                }
+            }
+            __syncthreads();
+            // ---- Tinv, diagonal blocks: thread j < Lp solves column j of its block
+            if (tid < Lp) {
+                const int j = tid, kb = j >> 4, c = j & 15;
+                float x[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) x[i] = i == c ? 1.f : 0.f;
+#pragma unroll
+                for (int l = 0; l < 15; ++l) {
+                    if (l >= c) {
+                        const float xl = x[l];
+                        const float4 *arow = reinterpret_cast<const float4 *>(sAt + (16 * kb + l) * CMAX + 16 * kb);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float4 av = arow[q];
+                            if (4 * q > l) x[4 * q] = fmaf(-av.x, xl, x[4 * q]);
+                            if (4 * q + 1 > l) x[4 * q + 1] = fmaf(-av.y, xl, x[4 * q + 1]);
+                            if (4 * q + 2 > l) x[4 * q + 2] = fmaf(-av.z, xl, x[4 * q + 2]);
+                            if (4 * q + 3 > l) x[4 * q + 3] = fmaf(-av.w, xl, x[4 * q + 3]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < CMAX; ++i) {                  // the whole column (zeros off the block)
+                    const int ib = i >> 4;
+                    sTi[i * CMAX + j] = ib == kb ? x[i & 15] : 0.f;
+                }
+            }
+            __syncthreads();
+            // ---- blocks below the diagonal, one block diagonal d at a time:
+            //      Y_j = sum_{k=j}^{j+d-1} A_{j+d,k} T_{k,j};  T_{j+d,j} = -T_{j+d,j+d} Y_j
+            for (int d = 1; d < nb; ++d) {
+                const int nblk = nb - d;
+                // a task: block j, row r, columns 4 c4 .. 4 c4 + 3
+                for (int e = tid; e < nblk * 64; e += kThreads) {
+                    const int j = e >> 6, r = (e >> 2) & 15, c4 = e & 3, i = j + d;
+                    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int k = j; k < i; ++k) {
+#pragma unroll
+                        for (int l = 0; l < 16; ++l) {
+                            const float av = sAt[(16 * k + l) * CMAX + 16 * i + r];
+                            const float4 tv = *reinterpret_cast<const float4 *>(sTi + (16 * k + l) * CMAX + 16 * j + 4 * c4);
+                            y.x = fmaf(av, tv.x, y.x); y.y = fmaf(av, tv.y, y.y);
+                            y.z = fmaf(av, tv.z, y.z); y.w = fmaf(av, tv.w, y.w);
+                        }
+                    }
+                    *reinterpret_cast<float4 *>(sY + (j << 8) + r * 16 + 4 * c4) = y;
+                }
+                __syncthreads();
+                for (int e = tid; e < nblk * 64; e += kThreads) {
+                    const int j = e >> 6, r = (e >> 2) & 15, c4 = e & 3, i = j + d;
+                    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int l = 0; l < 16; ++l) {
+                        const float tv = sTi[(16 * i + r) * CMAX + 16 * i + l];
+                        const float4 yv = *reinterpret_cast<const float4 *>(sY + (j << 8) + l * 16 + 4 * c4);
+                        t.x = fmaf(tv, yv.x, t.x); t.y = fmaf(tv, yv.y, t.y);
+                        t.z = fmaf(tv, yv.z, t.z); t.w = fmaf(tv, yv.w, t.w);
+                    }
+                    *reinterpret_cast<float4 *>(sTi + (16 * i + r) * CMAX + 16 * j + 4 * c4) =
+                        make_float4(-t.x, -t.y, -t.z, -t.w);
+                }
+                __syncthreads();
+            }
+            // ---- F[s'][s] = D_s Tinv[s][s'] as two bf16 K-major tiles [Lp][64]
+            for (int e = tid; e < Lp * 64 / 8; e += kThreads) {
+                const int sp = e >> 3, c8 = e & 7;                // row s', 8 columns s = 8 c8 ..
+                __nv_bfloat16 hh[8], ll[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int s = c8 * 8 + j;
+                    const float v = s < CMAX ? sD[s] * sTi[s * CMAX + sp] : 0.f;
+                    split2(v, hh[j], ll[j]);
+                }
+                const uint32_t off = sw128(sp, c8);
+                *reinterpret_cast<uint4 *>(sF + off) =
+                    make_uint4(pack2(hh[0], hh[1]), pack2(hh[2], hh[3]), pack2(hh[4], hh[5]), pack2(hh[6], hh[7]));
+                *reinterpret_cast<uint4 *>(sF + CMAX * 128 + off) =
+                    make_uint4(pack2(ll[0], ll[1]), pack2(ll[2], ll[3]), pack2(ll[4], ll[5]), pack2(ll[6], ll[7]));
+            }
+            fence_proxy_async();
+            __syncthreads();
+            if (tid == 0) {                                       // E^T = K^T F^T (keys MN-major)
+                tc_fence_after();
+                const uint32_t idE = idesc_mn(1, 128, Lp) | kIdescMnMajorA;
+                for (int ks = 0; ks < nb; ++ks) {
+                    const uint64_t ak = desc_mn_sw128(k0 + ks * 2048, P::SUBK);
+                    mma_bf16(tmem + COL_E, ak, desc_sw128(f0 + ks * 32), idE, ks > 0);
+                    mma_bf16(tmem + COL_E, ak, desc_sw128(f0 + CMAX * 128 + ks * 32), idE, 1);
+                }
+                mma_commit(&bar[1]);
+            }
+            ok = mbar_wait(&bar[1], ph);
+            if (__syncthreads_or(!ok)) {
+                if (tid == 0) { mbar_wait(&bar[1], ph); atomicOr(a.status, kStatusTimeout); }
+                alive = false;
+                break;
+            }
+            tc_fence_after();
+            // the checkpoint quarters 0, 1 come in from L2 (F is no longer read)
+            if (tid == 0) {
+                fence_proxy_async();
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    mbar_expect_tx(&bar[2 + q], 16384);
+                    tma_load_2d(sBuf + q * 16384, &tm_state, q * 32, ytile, &bar[2 + q]);
+                }
+            }
+            // ---- E^T row d_k = tid as two bf16 terms, K-major [128][64] tiles
+#pragma unroll
+            for (int cb = 0; cb < CMAX / 16; ++cb) {
+                if (cb < nb) {
+                    float ev[16];
+                    tmem_ld16(lane_base + COL_E + cb * 16, ev);
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        __nv_bfloat16 hh[8], ll[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) split2(ev[8 * hf + j], hh[j], ll[j]);
+                        const uint32_t off = sw128(tid, 2 * cb + hf);
+                        *reinterpret_cast<uint4 *>(sEt + off) = make_uint4(pack2(hh[0], hh[1]), pack2(hh[2], hh[3]),
+                                                                           pack2(hh[4], hh[5]), pack2(hh[6], hh[7]));
+                        *reinterpret_cast<uint4 *>(sEt + 16384 + off) = make_uint4(
+                            pack2(ll[0], ll[1]), pack2(ll[2], ll[3]), pack2(ll[4], ll[5]), pack2(ll[6], ll[7]));
+                    }
+                }
+            }
+            // ---- S0 K^T, quarter by quarter (thread 0), into the K K^T columns
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t idP = idesc_mn(2, 128, Lp);
+                int loads[2] = {1, 1}, mmas = 0;
+                bool good = true;
+                for (int q = 0; q < 4; ++q) {
+                    const int bi = q & 1;
+                    if (!mbar_wait(&bar[2 + bi], q >> 1)) { good = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_tf32(tmem + COL_P, desc_sw128(buf0 + bi * 16384 + ks * 32),
+                                 desc_sw128(kf0 + q * P::KFSUB + ks * 32), idP, (q | ks) != 0);
+                    mma_commit(&bar[4 + q]);
+                    mmas = q + 1;
+                    if (q < 2) {
+                        if (!mbar_wait(&bar[4 + q], ph)) { good = false; break; }
+                        mbar_expect_tx(&bar[2 + bi], 16384);
+                        tma_load_2d(sBuf + bi * 16384, &tm_state, (q + 2) * 32, ytile, &bar[2 + bi]);
+                        ++loads[bi];
+                    }
+                }
+                if (!good) {
+                    for (int q = 0; q < mmas; ++q) mbar_wait(&bar[4 + q], ph);
+                    for (int i = 0; i < 2; ++i) mbar_wait(&bar[2 + i], (loads[i] - 1) & 1);
+                    *flag = 1;
+                }
+            }
+            __syncthreads();
+            ok = *flag == 0;
+            if (ok) ok = mbar_wait(&bar[7], ph);
+            if (__syncthreads_or(!ok)) {
+                if (tid == 0) {
+                    if (*flag == 0) mbar_wait(&bar[7], ph);
+                    atomicOr(a.status, kStatusTimeout);
+                }
+                alive = false;
+                break;
+            }
+            tc_fence_after();
+            // ---- R row d_v = tid: r_s = beta_s (v_s - gamma_s (S0 k_s)), two bf16 terms
+            {
+                const uint8_t *vcol = sV + (tid >> 6) * P::SUBV + (tid & 7) * 2;
+                const int vch = (tid & 63) >> 3;
+#pragma unroll
+                for (int cb = 0; cb < CMAX / 16; ++cb) {
+                    if (cb < nb) {
+                        float pk[16];
+                        tmem_ld16(lane_base + COL_P + cb * 16, pk);
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            __nv_bfloat16 hh[8], ll[8];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const int s = cb * 16 + 8 * hf + j;
+                                const float v = __bfloat162float(
+                                    *reinterpret_cast<const __nv_bfloat16 *>(vcol + sw128(s, vch)));
+                                split2(sBeta[s] * (v - sGam[s] * pk[8 * hf + j]), hh[j], ll[j]);
+                            }
+                            const uint32_t off = sw128(tid, 2 * cb + hf);
+                            *reinterpret_cast<uint4 *>(sR + off) = make_uint4(
+                                pack2(hh[0], hh[1]), pack2(hh[2], hh[3]), pack2(hh[4], hh[5]), pack2(hh[6], hh[7]));
+                            *reinterpret_cast<uint4 *>(sR + 16384 + off) = make_uint4(
+                                pack2(ll[0], ll[1]), pack2(ll[2], ll[3]), pack2(ll[4], ll[5]), pack2(ll[6], ll[7]));
+                        }
+                    }
+                }
+            }
+            fence_proxy_async();
+            __syncthreads();
+            if (tid == 0) {                                       // D = R E: hi.hi + hi.lo + lo.hi
+                tc_fence_after();
+                const uint32_t idF = idesc_mn(1, 128, 128);
+                for (int ks = 0; ks < nb; ++ks) {
+                    const uint64_t rh = desc_sw128(r0 + ks * 32), rl = desc_sw128(r0 + 16384 + ks * 32);
+                    const uint64_t eh = desc_sw128(e0 + ks * 32), el = desc_sw128(e0 + 16384 + ks * 32);
+                    mma_bf16(tmem + COL_F, rh, eh, idF, ks > 0);
+                    mma_bf16(tmem + COL_F, rh, el, idF, 1);
+                    mma_bf16(tmem + COL_F, rl, eh, idF, 1);
+                }
+                mma_commit(&bar[8]);
+            }
+            // rows 32 warp .. 32 warp + 31 of S0 (L2), 512 contiguous bytes per warp load,
+            // while the contraction runs
+            float4 *srow = reinterpret_cast<float4 *>(a.state_out + (unit * 128 + 32 * warp) * 128) + lane;
+            float4 x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[i] = srow[i * 32];
+            ok = mbar_wait(&bar[8], ph);
+            if (__syncthreads_or(!ok)) {
+                if (tid == 0) { mbar_wait(&bar[8], ph); atomicOr(a.status, kStatusTimeout); }
+                alive = false;
+                break;
+            }
+            tc_fence_after();
+            // the draft rows ([K_d; Q_d] as 32 rows, V_d) and gates, for the verify below
+            uint4 dkq[4], dvv[2];
+            float dgq = 0.f, dbq = 0.f;
+            const size_t drow0 = (static_cast<size_t>(b) * a.T * H + h) * 128;
+            if constexpr (DRAFT) {
+                const size_t dstride = static_cast<size_t>(H) * 128;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+                    const int t = r & 15;
+                    dkq[i] = make_uint4(0u, 0u, 0u, 0u);
+                    if (t < a.T)
+                        dkq[i] = __ldg(reinterpret_cast<const uint4 *>(
+                                           reinterpret_cast<const __nv_bfloat16 *>(r < 16 ? a.k : a.q) + drow0 +
+                                           static_cast<size_t>(t) * dstride) + c);
+                }
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+                    dvv[i] = make_uint4(0u, 0u, 0u, 0u);
+                    if (r < a.T)
+                        dvv[i] = __ldg(reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(a.v) +
+                                                                       drow0 + static_cast<size_t>(r) * dstride) + c);
+                }
+                if (warp == 0 && lane < a.T) {
+                    const size_t gi = (static_cast<size_t>(b) * a.T + lane) * H + h;
+                    dgq = a.g[gi];
+                    dbq = a.beta[gi];
+                }
+            }
+            // ---- D row tid into shared memory (swizzled rows), then S_L = gamma_{L-1} S0 + D
+            //      row by row with coalesced loads and stores
+#pragma unroll
+            for (int c0 = 0; c0 < 128; c0 += 16) {
+                float dd[16];
+                tmem_ld16(lane_base + COL_F + c0, dd);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int col = c0 + 4 * q;
+                    *reinterpret_cast<float4 *>(sNew + (col >> 5) * 16384 + sw128(tid, (col & 31) >> 2)) =
+                        make_float4(dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
+                }
+            }
+            __syncwarp();                                         // a warp reads back only its own rows
+            {
+                const float gL = sGam[L - 1];
+                const uint8_t *dsub = sNew + (lane >> 3) * 16384;
+                float4 x2[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) x2[i] = srow[(16 + i) * 32];
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int row = 16 * hf + i;
+                        const float4 dv4 = *reinterpret_cast<const float4 *>(dsub + sw128(32 * warp + row, lane & 7));
+                        float4 y = hf ? x2[i] : x[i];
+                        y.x = fmaf(gL, y.x, dv4.x);
+                        y.y = fmaf(gL, y.y, dv4.y);
+                        y.z = fmaf(gL, y.z, dv4.z);
+                        y.w = fmaf(gL, y.w, dv4.w);
+                        srow[row * 32] = y;
+                        if constexpr (DRAFT)                     // S_L stays as the operand of the draft
+                            *reinterpret_cast<float4 *>(const_cast<uint8_t *>(dsub) + sw128(32 * warp + row, lane & 7)) = y;
+                    }
+                }
+            }
+            if constexpr (DRAFT) {
+                // ---- the draft, verified from the new state S_L (buffer now empty): with G'
+                //      the running sum over the draft alone, u' from the 16-token system and
+                //      o_t2 = scale (gamma'_t2 S_L q_t2 + sum_{s<=t2} e^{G'_t2-G'_s} (q_t2.k_s) u'_s);
+                //      the draft is staged at buffer slot 0
+                const int T = a.T;
+                uint8_t *sDq = sR;                                // [K_d; Q_d] fp32, 4 sub-tiles of 32 x 128 B
+                __nv_bfloat16 *sVd = reinterpret_cast<__nv_bfloat16 *>(sR + 16384);   // [16][128]
+                float *sAtd = reinterpret_cast<float *>(sR + 20480);                  // A'^T [16][16]
+                float *sMtd = sAtd + 256;                                             // M'^T [16][16]
+                float *sUd = reinterpret_cast<float *>(sR + 22528);                   // u' [16][128]
+                __nv_bfloat16 *wk = reinterpret_cast<__nv_bfloat16 *>(a.buf_k) + unit * cap * 128;
+                __nv_bfloat16 *wv = reinterpret_cast<__nv_bfloat16 *>(a.buf_v) + unit * cap * 128;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+                    float fl[8];
+                    bf16x8_to_f32(dkq[i], fl);
+                    uint8_t *tile = sDq + (c >> 2) * 4096;
+                    const int ch = (c & 3) * 2;
+                    *reinterpret_cast<float4 *>(tile + sw128(r, ch)) = make_float4(fl[0], fl[1], fl[2], fl[3]);
+                    *reinterpret_cast<float4 *>(tile + sw128(r, ch + 1)) = make_float4(fl[4], fl[5], fl[6], fl[7]);
+                    if (r < T) reinterpret_cast<uint4 *>(wk + static_cast<size_t>(r) * 128)[c] = dkq[i];
+                }
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+                    reinterpret_cast<uint4 *>(sVd + static_cast<size_t>(r) * 128)[c] = dvv[i];
+                    if (r < T) reinterpret_cast<uint4 *>(wv + static_cast<size_t>(r) * 128)[c] = dvv[i];
+                }
+                if (warp == 0) {                                  // compensated scan over the draft
+                    float hi = dgq, lo = 0.f;
+#pragma unroll
+                    for (int off = 1; off < 16; off <<= 1) {
+                        const float h2 = __shfl_up_sync(0xffffffffu, hi, off);
+                        const float l2 = __shfl_up_sync(0xffffffffu, lo, off);
+                        if (lane >= off) {
+                            const float s1 = hi + h2, bp = s1 - hi;
+                            lo += l2 + ((hi - (s1 - bp)) + (h2 - bp));
+                            hi = s1;
+                        }
+                    }
+                    if (lane < 16) {
+                        const bool live = lane < T;
+                        dGh[lane] = live ? hi : 0.f;
+                        dGl[lane] = live ? lo : 0.f;
+                        dGam[lane] = live ? __expf(hi + lo) : 0.f;
+                        dBeta[lane] = live ? dbq : 0.f;
+                        if (live) {
+                            a.buf_g[unit * cap + lane] = dgq;
+                            a.buf_beta[unit * cap + lane] = dbq;
+                        }
+                    }
+                }
+                fence_proxy_async();
+                tc_fence_before();
+                __syncthreads();
+                const uint32_t dq0 = saddr(sDq), sn0 = saddr(sNew);
+                if (tid == 0) {                                   // [K_d;Q_d] K_d^T and S_L [K_d;Q_d]^T
+                    tc_fence_after();
+                    const uint32_t idK = idesc_mn(2, 128, 16), idP = idesc_mn(2, 128, 32);
+#pragma unroll
+                    for (int ks = 0; ks < 16; ++ks) {
+                        const uint64_t dd = desc_sw128(dq0 + (ks >> 2) * 4096 + (ks & 3) * 32);
+                        mma_tf32(tmem + 0, dd, dd, idK, ks > 0);
+                        mma_tf32(tmem + 16, desc_sw128(sn0 + (ks >> 2) * 16384 + (ks & 3) * 32), dd, idP, ks > 0);
+                    }
+                    mma_commit(&bar[9]);
+                }
+                ok = mbar_wait(&bar[9], ph);
+                if (__syncthreads_or(!ok)) {
+                    if (tid == 0) { mbar_wait(&bar[9], ph); atomicOr(a.status, kStatusTimeout); }
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
+                if (warp == 0) {                                  // lanes 0..15: A' rows, 16..31: M' rows
+                    float kq[16];
+                    tmem_ld16(lane_base + 0, kq);
+                    const bool is_q = lane >= 16;
+                    const int t = lane & 15;
+                    const float gh = dGh[t], gl = dGl[t], scl = is_q ? 1.f : dBeta[t];
+                    const int lim = t >= T ? 0 : is_q ? t + 1 : t;
+                    float *dst = (is_q ? sMtd : sAtd) + t;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float e = __expf((gh - dGh[j]) + (gl - dGl[j]));
+                        dst[j * 16] = j < lim ? scl * e * kq[j] : 0.f;
+                    }
+                }
+                __syncthreads();
+                float od[16];
+                blocked_solve(T, tid, lane_base + 16, sAtd, 16, sMtd, sVd, sUd, dBeta, dGam, od);
+                float pq[16];
+                tmem_ld16(lane_base + 32, pq);
+#pragma unroll
+                for (int t2 = 0; t2 < 16; ++t2)
+                    if (t2 < T)
+                        a.out[((static_cast<size_t>(b) * T + t2) * H + h) * 128 + tid] =
+                            a.scale * (dGam[t2] * pq[t2] + od[t2]);
+            }
+            tc_fence_before();
+            __syncthreads();                                      // the tiles are reused by the next item
+        }
+        __syncthreads();                                          // the list is rebuilt
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1685,6 +2375,20 @@ int launch_verify(const gdn_replay_dims *d, const ReplayArgs &a0, const CUtensor
                                                                                        : GDN_ERR_LAUNCH;
 }
 
+template <bool DRAFT>
+int launch_fold(const gdn_replay_dims *d, const ReplayArgs &a, const CUtensorMap &m, cudaStream_t s) {
+    const bool small = d->cap <= 48;
+    const int smem = small ? FoldPlan<48>::BYTES : FoldPlan<64>::BYTES;
+    auto kern = small ? fold_eq_kernel<48, DRAFT> : fold_eq_kernel<64, DRAFT>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return GDN_ERR_LAUNCH;
+    int ctas = resident_ctas(reinterpret_cast<const void *>(kern), smem);
+    if (ctas <= 0) return GDN_ERR_LAUNCH;
+    ctas = ctas < d->B * d->H ? ctas : d->B * d->H;
+    return launch_pdl(kern, dim3(ctas), dim3(kThreads), smem, s, m, a) == cudaSuccess ? GDN_OK
+                                                                                 : GDN_ERR_LAUNCH;
+}
+
 }  // namespace
 
 int tc_verify(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s, bool fold) {
@@ -1698,36 +2402,27 @@ int tc_verify(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s, boo
     return cmax <= 48 ? launch_verify<48, true>(d, a, m, s) : launch_verify<64, true>(d, a, m, s);
 }
 
-int tc_verify_fold_split(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s) {
-    if (d->dk != 128 || d->dv != 128 || d->in_dtype != GDN_DTYPE_BF16) return 1;
-    const int cmax = d->cap + d->T;
-    if (cmax > 64 || d->T > 16 || d->cap > 48) return 1;
-    if (verify_smem_bytes(cmax, d->T) > 227 * 1024) return 1;
-    CUtensorMap m;
-    if (!state_map(&m, a.state_in, d->n_slot * d->H * 128)) return 1;
-    ReplayArgs af = a;
-    af.fold_class = 2;                                            // folding units, waits for earlier kernels
-    int rc = cmax <= 48 ? launch_verify<48, true>(d, af, m, s) : launch_verify<64, true>(d, af, m, s);
-    if (rc) return rc;
-    ReplayArgs an = a;
-    an.fold_class = 1;                                            // the rest, beside the fold launch
-    return launch_eq<48>(d, an, m, s);
-}
 
 int tc_flush(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s) {
     if (d->dk != 128 || d->dv != 128 || d->in_dtype != GDN_DTYPE_BF16) return 1;
-    if (d->cap > 64 || flush_smem_bytes(d->cap) > 227 * 1024) return 1;
+    if (d->cap > 64) return 1;
     CUtensorMap m;
     if (!state_map(&m, a.state_out, d->n_slot * d->H * 128)) return 1;
-    const int smem = flush_smem_bytes(d->cap);
-    auto kern = d->cap <= 48 ? flush_tc_kernel<48> : flush_tc_kernel<64>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return GDN_ERR_LAUNCH;
-    int ctas = resident_ctas(reinterpret_cast<const void *>(kern), smem);
-    if (ctas <= 0) return GDN_ERR_LAUNCH;
-    ctas = ctas < d->B * d->H ? ctas : d->B * d->H;
-    return launch_pdl(kern, dim3(ctas), dim3(kThreads), smem, s, m, a) == cudaSuccess ? GDN_OK
-                                                                                 : GDN_ERR_LAUNCH;
+    return launch_fold<false>(d, a, m, s);
+}
+
+int tc_verify_fold_split(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s) {
+    if (d->dk != 128 || d->dv != 128 || d->in_dtype != GDN_DTYPE_BF16) return 1;
+    if (d->cap > 64 || d->T > 16) return 1;
+    CUtensorMap m;
+    if (!state_map(&m, a.state_out, d->n_slot * d->H * 128)) return 1;
+    ReplayArgs af = a;                                            // fold the full buffers, verify the draft
+    af.force = 0;
+    const int rc = launch_fold<true>(d, af, m, s);
+    if (rc) return rc;
+    ReplayArgs an = a;                                            // the rest, beside the fold launch
+    an.fold_class = 1;
+    return d->cap <= 48 ? launch_eq<48>(d, an, m, s) : launch_eq<64>(d, an, m, s);
 }
 
 }  // namespace gdn
