@@ -397,7 +397,7 @@ int gdn_replay_verify(const gdn_replay_dims *d, const float *state, const int32_
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = out; a.status = status;
     a.B = d->B; a.H = d->H; a.T = d->T; a.cap = d->cap; a.threshold = d->threshold;
     a.n_slot = d->n_slot; a.scale = d->scale;
-    const int tc = gdn::tc_verify(d, a, stream, false);
+    const int tc = gdn::tc_verify(d, a, stream);
     if (tc <= 0) return tc;
     return dispatch_replay<kVerify>(d, a, stream);
 }
@@ -461,9 +461,7 @@ int gdn_replay_verify_fold(const gdn_replay_dims *d, float *state, const int32_t
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = out; a.status = status;
     a.B = d->B; a.H = d->H; a.T = d->T; a.cap = d->cap; a.threshold = d->threshold;
     a.n_slot = d->n_slot; a.scale = d->scale;
-    int tc = gdn::tc_verify_fold_split(d, a, stream);
-    if (tc <= 0) return tc;
-    tc = gdn::tc_verify(d, a, stream, true);
+    const int tc = gdn::tc_verify_fold(d, a, stream);
     if (tc <= 0) return tc;
     return dispatch_replay<kVerifyFold>(d, a, stream);
 }

@@ -23,9 +23,8 @@ struct ReplayArgs {
     int32_t *status;
     int B, H, T, cap, threshold, force, n_slot;
     float scale;
-    int prefetch_stride;        // > 0: CTA i prefetches into L2 the unit of CTA i + stride
-    int fold_class;             // 0: all units; 2: only units that fold; 1: only units that do not
-                                // fold, launched beside a fold_class 2 launch
+    int fold_class;             // 0: all units; 1: only the units that do not fold, launched
+                                // beside the fold launch
 };
 
 // Programmatic dependent launch: every kernel of the library is launched with
@@ -55,15 +54,14 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 // affected unit is skipped; nothing hangs).
 constexpr int32_t kStatusTimeout = GDN_STATUS_TIMEOUT;
 
-// Tensor-core path (gdn_replay_tc.cu).  Each returns GDN_OK when it launched,
-// GDN_ERR_LAUNCH on a launch failure, and 1 when the shape is not one it
-// handles (the caller then uses the per-token kernels).
-// fold = true: units whose buffer reached the threshold also write the checkpoint
-// after their buffered tokens and stage the draft at buffer slot 0.
-int tc_verify(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s, bool fold);
+// Tensor-core path (gdn_replay_tc.cu): d_k = d_v = 128, bf16 inputs, T <= 16,
+// cap <= 64.  Each returns GDN_OK when it launched, GDN_ERR_LAUNCH on a launch
+// failure, and 1 when the shape is not one it handles (the caller then uses the
+// per-token kernels).
+int tc_verify(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s);
 int tc_flush(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s);
-// Verify with fold as two launches on one stream: the folding sequences (two-CTA
-// kernel) and, running beside it, every other sequence (four-CTA kernel).
-int tc_verify_fold_split(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s);
+// The fused step: the folding sequences (persistent fold kernel, which then verifies
+// their drafts) and, beside it, the effective-query verify of every other sequence.
+int tc_verify_fold(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s);
 
 }  // namespace gdn
