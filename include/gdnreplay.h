@@ -4,15 +4,15 @@
  * hand-written CUDA kernels for sm_103a (GB300).
  *
  * Method ("The inference stack behind OCRia", LlamaIndex engineering blog,
- * section "Making speculative verification cheaper"): a GDN layer summarises
- * history in a fixed-size recurrent state that each token reads from HBM,
- * updates and writes back.  ReplaySSM instead keeps a checkpoint of the state
- * plus a small buffer of recent inputs, computes outputs from the checkpoint
- * and the buffered inputs, updates the full checkpoint only at a periodic
- * flush, and on rejection moves the buffer pointer so that only the accepted
- * prefix stays (no full-state restore).  The acceptance rule keeps the draft
- * tokens before the first rejected one ("Inference Engineering", chapter 5,
- * speculative decoding).
+ * section "Making speculative verification cheaper"): the recurrent state of a
+ * GDN layer is large, so moving it per token (and restoring it after a rejected
+ * draft) costs HBM traffic.  ReplaySSM keeps, per sequence, a checkpoint of the
+ * state and a short buffer of the inputs committed since; the draft's outputs
+ * come from replaying that buffer and the draft over the checkpoint, the
+ * checkpoint itself is rewritten only when the buffer is flushed, and a
+ * rejection only moves the buffer's length back.  Drafts are accepted up to the
+ * first rejected token ("Inference Engineering", chapter 5, speculative
+ * decoding).
  *
  * Recurrence (the gated delta rule of "Gated Delta Networks", Yang, Kautz &
  * Hatamizadeh, ICLR 2025; the blog names GDN without printing it), per
@@ -91,8 +91,9 @@ typedef struct {
 } gdn_replay_dims;
 
 /*
- * gdn_replay_verify -- "computes outputs from the checkpoint and the buffered
- * inputs" (blog, "Making speculative verification cheaper").
+ * gdn_replay_verify -- the verify pass of the blog's section "Making
+ * speculative verification cheaper": draft outputs from the checkpoint replayed
+ * with the buffered inputs.
  * For every b with slot s = state_idx[b] and len = buf_len[s], and every head:
  * start from state[s,h], replay the len committed tokens of the buffer, then
  * the T draft tokens, writing o_t = S_t (scale q_t) to out[b,t,h,:] for each
@@ -110,8 +111,8 @@ int gdn_replay_verify(const gdn_replay_dims *dims,
                       float *out, int32_t *status, cudaStream_t stream);
 
 /*
- * gdn_replay_accept -- rollback/commit "adjusts the buffer pointer to keep the
- * accepted prefix" (blog, same section): buf_len[s] += accepted[b] when
+ * gdn_replay_accept -- rollback and commit as a length update only (blog, same
+ * section: no state is restored): buf_len[s] += accepted[b] when
  * 0 <= accepted[b] <= T and the result fits in cap; rejected draft tokens stay
  * in the buffer as stale slots that the next verify overwrites.  Otherwise a
  * status bit is set and buf_len[s] is left unchanged.  Writes only buf_len.
@@ -121,8 +122,8 @@ int gdn_replay_accept(const gdn_replay_dims *dims, int32_t *buf_len,
                       int32_t *status, cudaStream_t stream);
 
 /*
- * gdn_replay_flush -- "updates the full checkpoint only at periodic flush"
- * (blog, same section).  For every b whose len = buf_len[s] satisfies
+ * gdn_replay_flush -- the periodic rewrite of the checkpoint (blog, same
+ * section).  For every b whose len = buf_len[s] satisfies
  * len >= threshold, or len > 0 when force != 0: replay the len buffered tokens
  * onto state[s,h] for every head, write the result back in place (fp32) and set
  * buf_len[s] = 0.  Other sequences are left bit-identical.  A len outside

@@ -7,13 +7,12 @@
  * or table with the CUDA library it checks.
  *
  * What it computes (sources: "The inference stack behind OCRia" (LlamaIndex
- * engineering blog), section "Making speculative verification cheaper":
- * GDN keeps a fixed-size recurrent state; ReplaySSM keeps a checkpoint of that
- * state plus a small buffer of recent inputs, computes outputs from the
- * checkpoint and the buffered inputs, updates the full checkpoint only at a
- * periodic flush, and on rejection moves the buffer pointer so only the
- * accepted prefix stays; "Inference Engineering", chapter 5, speculative
- * decoding: every draft token after the first rejected one is discarded).
+ * engineering blog), section "Making speculative verification cheaper": per
+ * sequence a checkpoint of the GDN state and a short buffer of the inputs
+ * committed since; draft outputs come from replaying buffer and draft over the
+ * checkpoint, the checkpoint is rewritten only when the buffer is flushed, and
+ * a rejection only shortens the buffer; "Inference Engineering", chapter 5,
+ * speculative decoding: drafts are accepted up to the first rejected token).
  *
  * The pages do not print the GDN recurrence; it is the gated delta rule of
  * Yang, Kautz & Hatamizadeh, "Gated Delta Networks" (ICLR 2025):

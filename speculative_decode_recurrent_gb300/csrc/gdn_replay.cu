@@ -3,9 +3,9 @@
 // include/gdnreplay.h; this file holds the kernels and host validation.
 //
 // Method: "The inference stack behind OCRia" (LlamaIndex engineering blog),
-// section "Making speculative verification cheaper" -- checkpoint + buffer of
-// recent inputs, outputs from checkpoint and buffered inputs, full checkpoint
-// updated only at flush, rollback as a buffer-pointer move.  Recurrence: the
+// section "Making speculative verification cheaper" -- a checkpoint of the state
+// and a buffer of committed inputs per sequence; verify replays both, flush
+// rewrites the checkpoint, accept moves the buffer length.  Recurrence: the
 // gated delta rule of "Gated Delta Networks" (ICLR 2025),
 //     S_t = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T,  o_t = S_t (scale q_t).
 //
