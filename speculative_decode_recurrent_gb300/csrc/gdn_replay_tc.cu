@@ -132,6 +132,12 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
            (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
            (static_cast<uint64_t>(2) << 61);
 }
+// A descriptor for the same layout `bytes` further on (the start-address field holds
+// address / 16 in 14 bits; shared-memory offsets here stay far below 256 KB).  Issue
+// sequences precompute their base descriptors and add constants: building each
+// 64-bit descriptor from scratch made every MMA issue cost ~150 cycles of
+// dependent integer work in the issuing thread.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 // Instruction descriptor: fp32 accumulator, A/B format `fmt` (tf32 = 2, bf16 = 1),
 // both K-major, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_mn(int fmt, int M, int N) {
@@ -489,9 +495,10 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
 #pragma unroll
         for (int q = 0; q < 4; ++q) prefetch_tile_l2(&tm_state, q * 32, ytile);
         const uint32_t idK = idesc_mn(1, 128, CP);
+        const uint64_t dkq = desc_sw128(kq0);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t d = desc_sw128(kq0 + (ks >> 2) * P::SUBK + (ks & 3) * 32);
+            const uint64_t d = desc_add(dkq, (ks >> 2) * P::SUBK + (ks & 3) * 32);
             mma_bf16(tmem, d, d, idK, ks > 0);
         }
         mma_commit(&bar[2]);
@@ -608,15 +615,15 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
         tc_fence_after();
         const uint32_t idQ = idesc_mn(1, 128, 16) | kIdescMnMajorA;
         const int nks = CP / 16;
+        const uint64_t dk = desc_mn_sw128(kq0, P::SUBK), dv = desc_mn_sw128(v0, P::SUBV), dw = desc_sw128(w0);
 #pragma unroll
         for (int ks = 0; ks < CMAX / 16; ++ks) {
             if (ks < nks) {
-                const uint64_t ak = desc_mn_sw128(kq0 + ks * 2048, P::SUBK);
-                const uint64_t av = desc_mn_sw128(v0 + ks * 2048, P::SUBV);
+                const uint64_t ak = desc_add(dk, ks * 2048), av = desc_add(dv, ks * 2048);
 #pragma unroll
                 for (int sp = 0; sp < 2; ++sp) {
-                    mma_bf16(tmem + COL_Q, ak, desc_sw128(w0 + sp * 2048 + ks * 32), idQ, (sp | ks) != 0);
-                    mma_bf16(tmem + COL_V, av, desc_sw128(w0 + (2 + sp) * 2048 + ks * 32), idQ, (sp | ks) != 0);
+                    mma_bf16(tmem + COL_Q, ak, desc_add(dw, sp * 2048 + ks * 32), idQ, (sp | ks) != 0);
+                    mma_bf16(tmem + COL_V, av, desc_add(dw, (2 + sp) * 2048 + ks * 32), idQ, (sp | ks) != 0);
                 }
             }
         }
@@ -656,24 +663,31 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     if (tid == 0) {                                               // O = S0 qe^T, quarter by quarter
         tc_fence_after();
         const uint32_t idO = idesc_mn(2, 128, 16);
+        const uint64_t ds0 = desc_sw128(s00), dqe = desc_sw128(qe0);
         int loads[2] = {1, 1};                                    // TMA loads issued per buffer
         int mmas = 0;                                             // quarters whose MMAs were issued
         bool good = true;
+#pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int buf = q & 1;
-            if (!mbar_wait(&bar[buf], q >> 1)) { good = false; break; }
-            tc_fence_after();
+            if (good && !mbar_wait(&bar[buf], q >> 1)) good = false;
+            if (good) {
+                tc_fence_after();
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_tf32(tmem + COL_O, desc_sw128(s00 + buf * 16384 + ks * 32),
-                         desc_sw128(qe0 + q * 2048 + ks * 32), idO, (q | ks) != 0);
-            mma_commit(&bar[4 + q]);
-            mmas = q + 1;
-            if (q < 2) {                                          // the buffer is reused once its MMAs are done
-                if (!mbar_wait(&bar[4 + q], 0)) { good = false; break; }
-                mbar_expect_tx(&bar[buf], 16384);
-                tma_load_2d(smem_raw + buf * 16384, &tm_state, (q + 2) * 32, ytile, &bar[buf]);
-                ++loads[buf];
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_tf32(tmem + COL_O, desc_add(ds0, buf * 16384 + ks * 32), desc_add(dqe, q * 2048 + ks * 32),
+                             idO, (q | ks) != 0);
+                mma_commit(&bar[4 + q]);
+                mmas = q + 1;
+            }
+            if (good && q < 2) {                                  // the buffer is reused once its MMAs are done
+                if (!mbar_wait(&bar[4 + q], 0)) {
+                    good = false;
+                } else {
+                    mbar_expect_tx(&bar[buf], 16384);
+                    tma_load_2d(smem_raw + buf * 16384, &tm_state, (q + 2) * 32, ytile, &bar[buf]);
+                    ++loads[buf];
+                }
             }
         }
         if (!good) {                                              // wait (bounded) for what is in flight
@@ -824,6 +838,10 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
     pdl_release();
     const uint32_t k0 = saddr(sK), f0 = saddr(sF), kf0 = saddr(sKf), buf0 = saddr(sBuf), r0 = saddr(sR),
                    e0 = saddr(sEt), v0 = saddr(sV);
+    // base descriptors (issue sequences add constant offsets)
+    const uint64_t dK = desc_sw128(k0), dKmn = desc_mn_sw128(k0, P::SUBK), dF = desc_sw128(f0),
+                   dKf = desc_sw128(kf0), dBuf = desc_sw128(buf0), dR = desc_sw128(r0), dE = desc_sw128(e0),
+                   dVmn = desc_mn_sw128(v0, P::SUBV);
 
     uint32_t it = 0;                                              // items done by this CTA
     bool alive = true;
@@ -962,8 +980,8 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_tf32(tmem + COL_P, desc_sw128(buf0 + bi * 16384 + ks * 32),
-                             desc_sw128(kf0 + q * P::KFSUB + ks * 32), idP, (q | ks) != 0);
+                    mma_tf32(tmem + COL_P, desc_add(dBuf, bi * 16384 + ks * 32), desc_add(dKf, q * P::KFSUB + ks * 32),
+                             idP, (q | ks) != 0);
                 mma_commit(&bar[4 + q]);
                 pk_mmas = q + 1;
             };
@@ -980,7 +998,7 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                 const uint32_t idK = idesc_mn(1, 128, Lp);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t d = desc_sw128(k0 + (ks >> 2) * P::SUBK + (ks & 3) * 32);
+                    const uint64_t d = desc_add(dK, (ks >> 2) * P::SUBK + (ks & 3) * 32);
                     mma_bf16(tmem + COL_KK, d, d, idK, ks > 0);
                 }
                 mma_commit(&bar[0]);
@@ -1171,10 +1189,13 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
             if (tid == 0) {                                       // E^T = K^T F^T (keys MN-major)
                 tc_fence_after();
                 const uint32_t idE = idesc_mn(1, 128, Lp) | kIdescMnMajorA;
-                for (int ks = 0; ks < nb; ++ks) {
-                    const uint64_t ak = desc_mn_sw128(k0 + ks * 2048, P::SUBK);
-                    mma_bf16(tmem + COL_E, ak, desc_sw128(f0 + ks * 32), idE, ks > 0);
-                    mma_bf16(tmem + COL_E, ak, desc_sw128(f0 + CMAX * 128 + ks * 32), idE, 1);
+#pragma unroll
+                for (int ks = 0; ks < CMAX / 16; ++ks) {
+                    if (ks < nb) {
+                        const uint64_t ak = desc_add(dKmn, ks * 2048);
+                        mma_bf16(tmem + COL_E, ak, desc_add(dF, ks * 32), idE, ks > 0);
+                        mma_bf16(tmem + COL_E, ak, desc_add(dF, CMAX * 128 + ks * 32), idE, 1);
+                    }
                 }
                 mma_commit(&bar[1]);
             }
@@ -1209,15 +1230,18 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
             if (tid == 0) {                                       // D = V^T E' + R' E'
                 tc_fence_after();
                 const uint32_t idF = idesc_mn(1, 128, 128), idV = idF | kIdescMnMajorA;
-                for (int ks = 0; ks < nb; ++ks) {
-                    const uint64_t av = desc_mn_sw128(v0 + ks * 2048, P::SUBV);
-                    const uint64_t rh = desc_sw128(r0 + ks * 32), rl = desc_sw128(r0 + 16384 + ks * 32);
-                    const uint64_t eh = desc_sw128(e0 + ks * 32), el = desc_sw128(e0 + 16384 + ks * 32);
-                    mma_bf16(tmem + COL_F, av, eh, idV, ks > 0);
-                    mma_bf16(tmem + COL_F, av, el, idV, 1);
-                    mma_bf16(tmem + COL_F, rh, eh, idF, 1);
-                    mma_bf16(tmem + COL_F, rh, el, idF, 1);
-                    mma_bf16(tmem + COL_F, rl, eh, idF, 1);
+#pragma unroll
+                for (int ks = 0; ks < CMAX / 16; ++ks) {
+                    if (ks < nb) {
+                        const uint64_t av = desc_add(dVmn, ks * 2048);
+                        const uint64_t rh = desc_add(dR, ks * 32), rl = desc_add(dR, 16384 + ks * 32);
+                        const uint64_t eh = desc_add(dE, ks * 32), el = desc_add(dE, 16384 + ks * 32);
+                        mma_bf16(tmem + COL_F, av, eh, idV, ks > 0);
+                        mma_bf16(tmem + COL_F, av, el, idV, 1);
+                        mma_bf16(tmem + COL_F, rh, eh, idF, 1);
+                        mma_bf16(tmem + COL_F, rh, el, idF, 1);
+                        mma_bf16(tmem + COL_F, rl, eh, idF, 1);
+                    }
                 }
                 mma_commit(&bar[8]);
             }
@@ -1362,11 +1386,12 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                 if (tid == 0) {                                   // [K_d;Q_d] K_d^T and S_L [K_d;Q_d]^T
                     tc_fence_after();
                     const uint32_t idK = idesc_mn(2, 128, 16), idP = idesc_mn(2, 128, 32);
+                    const uint64_t ddq = desc_sw128(dq0), dsn = desc_sw128(sn0);
 #pragma unroll
                     for (int ks = 0; ks < 16; ++ks) {
-                        const uint64_t dd = desc_sw128(dq0 + (ks >> 2) * 4096 + (ks & 3) * 32);
+                        const uint64_t dd = desc_add(ddq, (ks >> 2) * 4096 + (ks & 3) * 32);
                         mma_tf32(tmem + 0, dd, dd, idK, ks > 0);
-                        mma_tf32(tmem + 16, desc_sw128(sn0 + (ks >> 2) * 16384 + (ks & 3) * 32), dd, idP, ks > 0);
+                        mma_tf32(tmem + 16, desc_add(dsn, (ks >> 2) * 16384 + (ks & 3) * 32), dd, idP, ks > 0);
                     }
                     mma_commit(&bar[9]);
                 }

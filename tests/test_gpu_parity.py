@@ -316,3 +316,25 @@ def test_flush_many_sequences_list_chunks():
     orc.flush(force=False)
     slots = init["state_idx"][sample].long().numpy()
     assert_close("state", to_np(gpu.t["state"])[slots], orc.state[slots])
+
+
+# --------------------------------------------- 64-token buffers (capacity 49..64)
+def _cap63(name):
+    import dataclasses
+    return dataclasses.replace(WL[name], name=name + "_cap63", threshold=48)   # cap = 48 - 1 + 16 = 63
+
+
+@pytest.mark.parametrize("name", ["b8", "edge"])
+def test_cap63_three_call(name):
+    """Buffers of up to 63 tokens: the 64-token variants of the verify and of the
+    fold (four 16-token blocks in the inverse)."""
+    pr = Pair(_cap63(name))
+    for s in range(14):
+        pr.step(s)
+
+
+@pytest.mark.parametrize("name", ["b8", "edge"])
+def test_cap63_fused(name):
+    pr = Pair(_cap63(name))
+    for s in range(14):
+        pr.fused_step(s)
