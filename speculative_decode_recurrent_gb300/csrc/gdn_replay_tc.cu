@@ -172,85 +172,6 @@ __device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
 }
 
 // ---------------------------------------------------------------------------
-// Forward substitution in blocks of 16 tokens (one state row per thread).
-//   u_t = beta_t (v_t - gamma_t P_t) - sum_{s<t} A[t][s] u_s,   t < C
-// and, when Mt is given, the draft sums o[t2] = sum_s M[t2][s] u_s.
-// Earlier blocks' u live in shared memory (this thread's column of sU), so the
-// cross-block update is a rolled loop and the unrolled code is one 16 x 16
-// triangle: the instruction stream stays small enough to be cached.
-//   At  [>= CP rows][LDT]  A transposed (At[s][t] = A[t][s]); zeros at s >= t
-//   Mt  [>= CP rows][16]   M transposed (Mt[s][t2] = M[t2][s]); zeros past p
-//   sV  [C][128] bf16      value rows;  sU [C][128] fp32 receives u
-//   P   TMEM columns [0, C) of this thread's lane (S0 k_t)
-// Tokens t >= C get u = 0 (their coefficient entries may be unset).
-__device__ __forceinline__ void blocked_solve(int C, int tid, uint32_t lane_base, const float *At, int LDT,
-                                              const float *Mt, const __nv_bfloat16 *sV, float *sU,
-                                              const float *sBeta, const float *sGam, float (&o)[16])
-{
-#pragma unroll
-    for (int j = 0; j < 16; ++j) o[j] = 0.f;
-    const int nb = (C + 15) >> 4;
-#pragma unroll 1
-    for (int kb = 0; kb < nb; ++kb) {
-        const int t0 = kb * 16;
-        float pc[16], r[16];
-        tmem_ld16(lane_base + t0, pc);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int t = t0 + j;
-            const float vt = t < C ? __bfloat162float(sV[static_cast<size_t>(t) * 128 + tid]) : 0.f;
-            r[j] = t < C ? sBeta[t] * (vt - sGam[t] * pc[j]) : 0.f;
-        }
-        // contributions of the earlier blocks
-#pragma unroll 2
-        for (int s = 0; s < t0; ++s) {
-            const float us = sU[static_cast<size_t>(s) * 128 + tid];
-            const float4 *a4 = reinterpret_cast<const float4 *>(At + static_cast<size_t>(s) * LDT + t0);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 x = a4[q];
-                r[4 * q] = fmaf(-x.x, us, r[4 * q]);
-                r[4 * q + 1] = fmaf(-x.y, us, r[4 * q + 1]);
-                r[4 * q + 2] = fmaf(-x.z, us, r[4 * q + 2]);
-                r[4 * q + 3] = fmaf(-x.w, us, r[4 * q + 3]);
-            }
-        }
-        // the 16 x 16 triangle of this block, right-looking
-#pragma unroll
-        for (int jp = 0; jp < 16; ++jp) {
-            const float uj = (t0 + jp < C) ? r[jp] : 0.f;
-            r[jp] = uj;
-            const float4 *a4 = reinterpret_cast<const float4 *>(At + static_cast<size_t>(t0 + jp) * LDT + t0);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 x = a4[q];
-                if (4 * q > jp) r[4 * q] = fmaf(-x.x, uj, r[4 * q]);
-                if (4 * q + 1 > jp) r[4 * q + 1] = fmaf(-x.y, uj, r[4 * q + 1]);
-                if (4 * q + 2 > jp) r[4 * q + 2] = fmaf(-x.z, uj, r[4 * q + 2]);
-                if (4 * q + 3 > jp) r[4 * q + 3] = fmaf(-x.w, uj, r[4 * q + 3]);
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-            if (t0 + j < C) sU[static_cast<size_t>(t0 + j) * 128 + tid] = r[j];
-        if (Mt) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float4 *m4 = reinterpret_cast<const float4 *>(Mt + static_cast<size_t>(t0 + j) * 16);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 x = m4[q];
-                    o[4 * q] = fmaf(x.x, r[j], o[4 * q]);
-                    o[4 * q + 1] = fmaf(x.y, r[j], o[4 * q + 1]);
-                    o[4 * q + 2] = fmaf(x.z, r[j], o[4 * q + 2]);
-                    o[4 * q + 3] = fmaf(x.w, r[j], o[4 * q + 3]);
-                }
-            }
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
 // Verify by effective queries (no fold; T <= 16, C = len + T <= CMAX).
 //
 // The chunked form gives u = (I + A)^{-1} r with r_s = beta_s (v_s - gamma_s S0 k_s),
@@ -753,9 +674,10 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
 //   [OFF_V, +2 SUBV)       value rows, bf16
 //   [OFF_KF, +4 KFSUB)     key rows, fp32, 4 sub-tiles of CMAX rows x 128 B (S0 K^T);
 //                          then F as two bf16 tiles [CMAX][64]
-//   [OFF_Q, +32K)          the two checkpoint buffers; then R' as two bf16 tiles
-//                          [128][64]; in the draft verify, its tiles
-//   [0, 64K)               after the fold contraction: D, then S_L (rows, swizzled)
+//   [OFF_Q, +32K)          the two checkpoint buffers; then R' as two bf16 tiles [128][64]
+//   after the fold contraction: D, then S_L (rows, swizzled) in four 16 KB sub-tiles at
+//   [0, 32K) and [OFF_Q, +32K); draft (DRAFT): its token tiles in the fp32 key region
+//   (free once E' is formed) and qe over the value rows (free after the fold)
 //   [OFF_SC, ...)          mbarriers, TMEM slot, flags, G (hi, lo), beta, gamma, D, list
 template <int CMAX> struct FoldPlan {
     static constexpr int SUBK = CMAX * 128;
@@ -774,6 +696,8 @@ template <int CMAX> struct FoldPlan {
     static_assert(CMAX == 48 || CMAX == 64, "token blocks");
     static_assert(SUBK + 16384 <= OFF_SC, "M = 128 operand reads stay inside the allocation");
     static_assert(2 * CMAX * 128 <= 4 * KFSUB, "F over the fp32 key tile");
+    static_assert(4 * KFSUB >= 22528, "draft tiles in the fp32 key region");
+    static_assert(2 * SUBV >= 8192, "draft qe tile over the value rows");
     static_assert(OFF_V >= 32768 && OFF_V + 2 * SUBV + 4 * KFSUB <= OFF_Q, "E^T tiles below the values");
     static_assert(OFF_SC >= 65536, "staging of the new state");
     static_assert((OFF_V % 1024) == 0 && (OFF_KF % 1024) == 0 && (OFF_Q % 1024) == 0 && (SUBK % 1024) == 0 &&
@@ -803,14 +727,16 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
     float *sY = reinterpret_cast<float *>(smem_raw + P::OFF_Y);   // [3][16][16]
     uint8_t *sBuf = smem_raw + P::OFF_Q;                          // 2 x 16 KB
     uint8_t *sR = smem_raw + P::OFF_Q;                            // 2 x 16 KB
-    uint8_t *sNew = smem_raw;                                     // 64 KB
+    // the new state (D, then S_L), 4 sub-tiles of 16 KB: two over E'^T, two over R'
+    auto snew = [&](int k) -> uint8_t * { return smem_raw + (k < 2 ? k * 16384 : P::OFF_Q + (k - 2) * 16384); };
     uint8_t *sm = smem_raw + P::OFF_SC;
-    // 0: K.K; 1: E^T; 2, 3: checkpoint buffers; 4..7: S0 K^T quarters; 8: fold; 9: draft
+    // 0: K.K; 1: E^T; 2, 3: checkpoint buffers; 4..7: S0 K^T quarters; 8: fold;
+    // 9..11: draft (K_d K_d^T, qe/ve, S_L qe^T)
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + 80);
-    int *flag = reinterpret_cast<int *>(sm + 84);
-    int *n_list = reinterpret_cast<int *>(sm + 88);
-    int *warp_cnt = reinterpret_cast<int *>(sm + 96);              // [4]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + 96);
+    int *flag = reinterpret_cast<int *>(sm + 100);
+    int *n_list = reinterpret_cast<int *>(sm + 104);
+    int *warp_cnt = reinterpret_cast<int *>(sm + 112);             // [4]
     float *sGh = reinterpret_cast<float *>(sm + 128);
     float *sGl = sGh + CMAX;
     float *sBeta = sGl + CMAX;
@@ -825,7 +751,7 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
 
     if (tid == 0) {
 #pragma unroll
-        for (int i = 0; i < 10; ++i) mbar_init(&bar[i], 1);
+        for (int i = 0; i < 12; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
@@ -1245,31 +1171,32 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                 }
                 mma_commit(&bar[8]);
             }
-            // rows 32 warp .. 32 warp + 31 of S0 (L2), 512 contiguous bytes per warp load,
-            // while the contraction runs
-            float4 *srow = reinterpret_cast<float4 *>(a.state_out + (unit * 128 + 32 * warp) * 128) + lane;
-            float4 x[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = srow[i * 32];
-            ok = mbar_wait(&bar[8], ph);
-            if (__syncthreads_or(!ok)) {
-                if (tid == 0) { mbar_wait(&bar[8], ph); atomicOr(a.status, kStatusTimeout); }
-                alive = false;
-                break;
-            }
-            tc_fence_after();
-            // the draft rows ([K_d; Q_d] as 32 rows, V_d) and gates, for the verify below
-            uint4 dkq[4], dvv[2];
-            float dgq = 0.f, dbq = 0.f;
-            const size_t drow0 = (static_cast<size_t>(b) * a.T * H + h) * 128;
+            // ---- DRAFT (fused step): the draft is then verified from S_L (the buffer is
+            //      empty after the fold) by effective queries over the 16 draft tokens alone
+            //      (G' restarted at the draft): W' = M' (I + A')^{-1}, qe = gamma' q - (W' beta'
+            //      gamma') K_d, ve = (W' beta') V_d, o = scale (S_L qe + ve).  Everything but the
+            //      S_L contraction runs while the fold contraction executes; its tiles sit in
+            //      the fp32 key region (free since E' was formed), its accumulators in the TMEM
+            //      columns of S0 K^T.  The draft is staged at buffer slot 0.
+            constexpr int SUBKD = 4096, SUBVD = 2048;             // [K_d; Q_d] 32 rows, V_d 16 rows
+            uint8_t *sDKQ = sKf;                                  // 2 sub-tiles of 32 rows x 128 B
+            uint8_t *sVd = sKf + 8192;                            // 2 sub-tiles of 16 rows x 128 B
+            float *sAd = reinterpret_cast<float *>(sKf + 12288);  // A' [16][16]
+            float *sMd = sAd + 256;                               // M' [16][16]
+            uint8_t *sWd = sKf + 14336;                           // W' beta' gamma', W' beta': 2 + 2 tiles [16][64]
+            uint8_t *sQd = sV;                                    // qe, fp32 [16][128], after the fold
+            constexpr uint32_t COL_KD = 0, COL_DQ = 16, COL_DV = 32, COL_DO = 48;
             if constexpr (DRAFT) {
+                const int T = a.T;
+                const size_t drow0 = (static_cast<size_t>(b) * T * H + h) * 128;
                 const size_t dstride = static_cast<size_t>(H) * 128;
+                uint4 dkq[4], dvv[2];
+                float dgq = 0.f, dbq = 0.f;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
-                    const int t = r & 15;
+                    const int e = tid + i * kThreads, r = e >> 4, c = e & 15, t = r & 15;
                     dkq[i] = make_uint4(0u, 0u, 0u, 0u);
-                    if (t < a.T)
+                    if (t < T)
                         dkq[i] = __ldg(reinterpret_cast<const uint4 *>(
                                            reinterpret_cast<const __nv_bfloat16 *>(r < 16 ? a.k : a.q) + drow0 +
                                            static_cast<size_t>(t) * dstride) + c);
@@ -1278,81 +1205,27 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                 for (int i = 0; i < 2; ++i) {
                     const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
                     dvv[i] = make_uint4(0u, 0u, 0u, 0u);
-                    if (r < a.T)
+                    if (r < T)
                         dvv[i] = __ldg(reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(a.v) +
                                                                        drow0 + static_cast<size_t>(r) * dstride) + c);
                 }
-                if (warp == 0 && lane < a.T) {
-                    const size_t gi = (static_cast<size_t>(b) * a.T + lane) * H + h;
+                if (warp == 0 && lane < T) {
+                    const size_t gi = (static_cast<size_t>(b) * T + lane) * H + h;
                     dgq = a.g[gi];
                     dbq = a.beta[gi];
                 }
-            }
-            // ---- D row tid into shared memory (swizzled rows), then S_L = gamma_{L-1} S0 + D
-            //      row by row with coalesced loads and stores
-#pragma unroll
-            for (int c0 = 0; c0 < 128; c0 += 16) {
-                float dd[16];
-                tmem_ld16(lane_base + COL_F + c0, dd);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int col = c0 + 4 * q;
-                    *reinterpret_cast<float4 *>(sNew + (col >> 5) * 16384 + sw128(tid, (col & 31) >> 2)) =
-                        make_float4(dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
-                }
-            }
-            __syncwarp();                                         // a warp reads back only its own rows
-            {
-                const float gL = sGam[L - 1];
-                const uint8_t *dsub = sNew + (lane >> 3) * 16384;
-                float4 x2[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) x2[i] = srow[(16 + i) * 32];
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int row = 16 * hf + i;
-                        const float4 dv4 = *reinterpret_cast<const float4 *>(dsub + sw128(32 * warp + row, lane & 7));
-                        float4 y = hf ? x2[i] : x[i];
-                        y.x = fmaf(gL, y.x, dv4.x);
-                        y.y = fmaf(gL, y.y, dv4.y);
-                        y.z = fmaf(gL, y.z, dv4.z);
-                        y.w = fmaf(gL, y.w, dv4.w);
-                        srow[row * 32] = y;
-                        if constexpr (DRAFT)                     // S_L stays as the operand of the draft
-                            *reinterpret_cast<float4 *>(const_cast<uint8_t *>(dsub) + sw128(32 * warp + row, lane & 7)) = y;
-                    }
-                }
-            }
-            if constexpr (DRAFT) {
-                // ---- the draft, verified from the new state S_L (buffer now empty): with G'
-                //      the running sum over the draft alone, u' from the 16-token system and
-                //      o_t2 = scale (gamma'_t2 S_L q_t2 + sum_{s<=t2} e^{G'_t2-G'_s} (q_t2.k_s) u'_s);
-                //      the draft is staged at buffer slot 0
-                const int T = a.T;
-                uint8_t *sDq = sR;                                // [K_d; Q_d] fp32, 4 sub-tiles of 32 x 128 B
-                __nv_bfloat16 *sVd = reinterpret_cast<__nv_bfloat16 *>(sR + 16384);   // [16][128]
-                float *sAtd = reinterpret_cast<float *>(sR + 20480);                  // A'^T [16][16]
-                float *sMtd = sAtd + 256;                                             // M'^T [16][16]
-                float *sUd = reinterpret_cast<float *>(sR + 22528);                   // u' [16][128]
                 __nv_bfloat16 *wk = reinterpret_cast<__nv_bfloat16 *>(a.buf_k) + unit * cap * 128;
                 __nv_bfloat16 *wv = reinterpret_cast<__nv_bfloat16 *>(a.buf_v) + unit * cap * 128;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
-                    float fl[8];
-                    bf16x8_to_f32(dkq[i], fl);
-                    uint8_t *tile = sDq + (c >> 2) * 4096;
-                    const int ch = (c & 3) * 2;
-                    *reinterpret_cast<float4 *>(tile + sw128(r, ch)) = make_float4(fl[0], fl[1], fl[2], fl[3]);
-                    *reinterpret_cast<float4 *>(tile + sw128(r, ch + 1)) = make_float4(fl[4], fl[5], fl[6], fl[7]);
+                    *reinterpret_cast<uint4 *>(sDKQ + (c >> 3) * SUBKD + sw128(r, c & 7)) = dkq[i];
                     if (r < T) reinterpret_cast<uint4 *>(wk + static_cast<size_t>(r) * 128)[c] = dkq[i];
                 }
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
                     const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
-                    reinterpret_cast<uint4 *>(sVd + static_cast<size_t>(r) * 128)[c] = dvv[i];
+                    *reinterpret_cast<uint4 *>(sVd + (c >> 3) * SUBVD + sw128(r, c & 7)) = dvv[i];
                     if (r < T) reinterpret_cast<uint4 *>(wv + static_cast<size_t>(r) * 128)[c] = dvv[i];
                 }
                 if (warp == 0) {                                  // compensated scan over the draft
@@ -1380,52 +1253,192 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                     }
                 }
                 fence_proxy_async();
-                tc_fence_before();
                 __syncthreads();
-                const uint32_t dq0 = saddr(sDq), sn0 = saddr(sNew);
-                if (tid == 0) {                                   // [K_d;Q_d] K_d^T and S_L [K_d;Q_d]^T
+                if (tid == 0) {                                   // [K_d; Q_d] K_d^T
                     tc_fence_after();
-                    const uint32_t idK = idesc_mn(2, 128, 16), idP = idesc_mn(2, 128, 32);
-                    const uint64_t ddq = desc_sw128(dq0), dsn = desc_sw128(sn0);
+                    const uint32_t idK = idesc_mn(1, 128, 16);
+                    const uint64_t dkd = desc_sw128(saddr(sDKQ));
 #pragma unroll
-                    for (int ks = 0; ks < 16; ++ks) {
-                        const uint64_t dd = desc_add(ddq, (ks >> 2) * 4096 + (ks & 3) * 32);
-                        mma_tf32(tmem + 0, dd, dd, idK, ks > 0);
-                        mma_tf32(tmem + 16, desc_add(dsn, (ks >> 2) * 16384 + (ks & 3) * 32), dd, idP, ks > 0);
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t d = desc_add(dkd, (ks >> 2) * SUBKD + (ks & 3) * 32);
+                        mma_bf16(tmem + COL_KD, d, d, idK, ks > 0);
                     }
                     mma_commit(&bar[9]);
                 }
                 ok = mbar_wait(&bar[9], ph);
                 if (__syncthreads_or(!ok)) {
-                    if (tid == 0) { mbar_wait(&bar[9], ph); atomicOr(a.status, kStatusTimeout); }
+                    if (tid == 0) {
+                        mbar_wait(&bar[8], ph);
+                        mbar_wait(&bar[9], ph);
+                        atomicOr(a.status, kStatusTimeout);
+                    }
                     alive = false;
                     break;
                 }
                 tc_fence_after();
                 if (warp == 0) {                                  // lanes 0..15: A' rows, 16..31: M' rows
                     float kq[16];
-                    tmem_ld16(lane_base + 0, kq);
+                    tmem_ld16(lane_base + COL_KD, kq);
                     const bool is_q = lane >= 16;
                     const int t = lane & 15;
                     const float gh = dGh[t], gl = dGl[t], scl = is_q ? 1.f : dBeta[t];
                     const int lim = t >= T ? 0 : is_q ? t + 1 : t;
-                    float *dst = (is_q ? sMtd : sAtd) + t;
+                    float *dst = (is_q ? sMd : sAd) + t * 16;
+                    float mrow[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const float e = __expf((gh - dGh[j]) + (gl - dGl[j]));
-                        dst[j * 16] = j < lim ? scl * e * kq[j] : 0.f;
+                        mrow[j] = j < lim ? scl * e * kq[j] : 0.f;
                     }
+#pragma unroll
+                    for (int j4 = 0; j4 < 4; ++j4)
+                        *reinterpret_cast<float4 *>(dst + 4 * j4) =
+                            make_float4(mrow[4 * j4], mrow[4 * j4 + 1], mrow[4 * j4 + 2], mrow[4 * j4 + 3]);
                 }
                 __syncthreads();
-                float od[16];
-                blocked_solve(T, tid, lane_base + 16, sAtd, 16, sMtd, sVd, sUd, dBeta, dGam, od);
-                float pq[16];
-                tmem_ld16(lane_base + 32, pq);
+                {                                                 // W' rows 4 warp .. 4 warp + 3, lane = column
+                    float xw[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) xw[i] = lane < 16 ? sMd[(4 * warp + i) * 16 + lane] : 0.f;
+                    for (int s2 = T - 1; s2 >= 0; --s2) {
+                        const float av = lane < 16 ? sAd[s2 * 16 + lane] : 0.f;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float w = __shfl_sync(0xffffffffu, xw[i], s2);
+                            xw[i] = fmaf(-w, av, xw[i]);
+                        }
+                    }
+                    if (lane < 16) {
+                        const float bs = dBeta[lane], bg = bs * dGam[lane];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            __nv_bfloat16 t4[4];
+                            split2(xw[i] * bg, t4[0], t4[1]);
+                            split2(xw[i] * bs, t4[2], t4[3]);
+                            const uint32_t off = sw128(4 * warp + i, lane >> 3) + (lane & 7) * 2;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) *reinterpret_cast<__nv_bfloat16 *>(sWd + j * 2048 + off) = t4[j];
+                        }
+                    }
+                }
+                fence_proxy_async();
+                __syncthreads();
+                if (tid == 0) {                                   // qe^T, ve^T (K_d, V_d MN-major)
+                    tc_fence_after();
+                    const uint32_t idQ = idesc_mn(1, 128, 16) | kIdescMnMajorA;
+                    const uint64_t ak = desc_mn_sw128(saddr(sDKQ), SUBKD), av = desc_mn_sw128(saddr(sVd), SUBVD);
+                    const uint64_t dw = desc_sw128(saddr(sWd));
+                    mma_bf16(tmem + COL_DQ, ak, dw, idQ, 0);
+                    mma_bf16(tmem + COL_DQ, ak, desc_add(dw, 2048), idQ, 1);
+                    mma_bf16(tmem + COL_DV, av, desc_add(dw, 4096), idQ, 0);
+                    mma_bf16(tmem + COL_DV, av, desc_add(dw, 6144), idQ, 1);
+                    mma_commit(&bar[10]);
+                }
+            }
+            // rows 32 warp .. 32 warp + 31 of S0 (L2), 512 contiguous bytes per warp load,
+            // while the contraction runs
+            float4 *srow = reinterpret_cast<float4 *>(a.state_out + (unit * 128 + 32 * warp) * 128) + lane;
+            float4 x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[i] = srow[i * 32];
+            ok = mbar_wait(&bar[8], ph);
+            if (__syncthreads_or(!ok)) {
+                if (tid == 0) {
+                    mbar_wait(&bar[8], ph);
+                    if (DRAFT) mbar_wait(&bar[10], ph);
+                    atomicOr(a.status, kStatusTimeout);
+                }
+                alive = false;
+                break;
+            }
+            tc_fence_after();
+            // ---- D row tid into shared memory (swizzled rows), then S_L = gamma_{L-1} S0 + D
+            //      row by row with coalesced loads and stores
+#pragma unroll
+            for (int c0 = 0; c0 < 128; c0 += 16) {
+                float dd[16];
+                tmem_ld16(lane_base + COL_F + c0, dd);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int col = c0 + 4 * q;
+                    *reinterpret_cast<float4 *>(snew(col >> 5) + sw128(tid, (col & 31) >> 2)) =
+                        make_float4(dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
+                }
+            }
+            __syncwarp();                                         // a warp reads back only its own rows
+            {
+                const float gL = sGam[L - 1];
+                const uint8_t *dsub = snew(lane >> 3);
+                float4 x2[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) x2[i] = srow[(16 + i) * 32];
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int row = 16 * hf + i;
+                        const float4 dv4 = *reinterpret_cast<const float4 *>(dsub + sw128(32 * warp + row, lane & 7));
+                        float4 y = hf ? x2[i] : x[i];
+                        y.x = fmaf(gL, y.x, dv4.x);
+                        y.y = fmaf(gL, y.y, dv4.y);
+                        y.z = fmaf(gL, y.z, dv4.z);
+                        y.w = fmaf(gL, y.w, dv4.w);
+                        srow[row * 32] = y;
+                        if constexpr (DRAFT)                     // S_L stays as the operand of the draft
+                            *reinterpret_cast<float4 *>(const_cast<uint8_t *>(dsub) + sw128(32 * warp + row, lane & 7)) = y;
+                    }
+                }
+            }
+            if constexpr (DRAFT) {
+                const int T = a.T;
+                ok = mbar_wait(&bar[10], ph);
+                if (__syncthreads_or(!ok)) {
+                    if (tid == 0) { mbar_wait(&bar[10], ph); atomicOr(a.status, kStatusTimeout); }
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
+                {                                                 // qe[t2][d_k = tid], fp32 K-major tile
+                    float dq[16];
+                    tmem_ld16(lane_base + COL_DQ, dq);
+                    uint8_t *col = sQd + (tid >> 5) * 2048 + (tid & 3) * 4;
+                    const uint8_t *qsrc = sDKQ + (tid >> 6) * SUBKD + (tid & 7) * 2;
+#pragma unroll
+                    for (int t2 = 0; t2 < 16; ++t2) {
+                        const float qv = __bfloat162float(
+                            *reinterpret_cast<const __nv_bfloat16 *>(qsrc + sw128(16 + t2, (tid & 63) >> 3)));
+                        const float v = t2 < T ? fmaf(dGam[t2], qv, -dq[t2]) : 0.f;
+                        *reinterpret_cast<float *>(col + sw128(t2, (tid & 31) >> 2)) = v;
+                    }
+                }
+                fence_proxy_async();
+                tc_fence_before();
+                __syncthreads();
+                if (tid == 0) {                                   // O = S_L qe^T (S_L from the staging tile)
+                    tc_fence_after();
+                    const uint32_t idO = idesc_mn(2, 128, 16);
+                    const uint64_t dsa = desc_sw128(saddr(snew(0))), dsb = desc_sw128(saddr(snew(2)));
+                    const uint64_t dqd = desc_sw128(saddr(sQd));
+#pragma unroll
+                    for (int ks = 0; ks < 16; ++ks)
+                        mma_tf32(tmem + COL_DO, desc_add(ks < 8 ? dsa : dsb, ((ks >> 2) & 1) * 16384 + (ks & 3) * 32),
+                                 desc_add(dqd, (ks >> 2) * 2048 + (ks & 3) * 32), idO, ks > 0);
+                    mma_commit(&bar[11]);
+                }
+                ok = mbar_wait(&bar[11], ph);
+                if (__syncthreads_or(!ok)) {
+                    if (tid == 0) { mbar_wait(&bar[11], ph); atomicOr(a.status, kStatusTimeout); }
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
+                float o[16], ve[16];
+                tmem_ld16(lane_base + COL_DO, o);
+                tmem_ld16(lane_base + COL_DV, ve);
 #pragma unroll
                 for (int t2 = 0; t2 < 16; ++t2)
                     if (t2 < T)
-                        a.out[((static_cast<size_t>(b) * T + t2) * H + h) * 128 + tid] =
-                            a.scale * (dGam[t2] * pq[t2] + od[t2]);
+                        a.out[((static_cast<size_t>(b) * T + t2) * H + h) * 128 + tid] = a.scale * (o[t2] + ve[t2]);
             }
             tc_fence_before();
             __syncthreads();                                      // the tiles are reused by the next item
