@@ -3,10 +3,10 @@
 tokens, flush threshold 32, accepted counts ~ geometric with mean 12 capped at
 16), on one GPU per rank.
 
-One step = for each of the 24 layers: gdn_replay_verify and gdn_replay_accept on
-the main stream, and gdn_replay_flush of that layer on a side stream (the flush
-of a layer is needed only by that layer's next verify, so it runs beside the
-following layers' verifies; the step ends with a join).  The same work in two
+One step = for each of the 24 layers: gdn_replay_verify on the main stream, and
+gdn_replay_accept + gdn_replay_flush of that layer on a side stream (they are
+needed only by that layer's next verify, so they run beside the following
+layers' verifies; the step ends with a join).  The same work in two
 other schedules is reported beside it: "three_call" (all three calls in order on
 one stream) and "fused" (gdn_replay_verify_fold + gdn_replay_accept_fold, the
 flush folded into the next verify).  Every layer keeps its own checkpoint and
@@ -212,23 +212,27 @@ def run_ours(args, rank, world, mode="fused"):
 
     fused = mode == "fused"
     overlap = mode == "overlap"        # three-call step, each layer's flush on a side stream
-    side = torch.cuda.Stream(device=dev)
+    sides = [torch.cuda.Stream(device=dev) for _ in range(2)]   # layers alternate between them
     fork = [torch.cuda.Event() for _ in range(L)]
 
     def enqueue_overlap(j, blocks=None, accs=None):
-        # verify and accept of every layer in order on the main stream; the flush of
-        # layer l (needed only by layer l's next verify, one step later) runs on a
-        # side stream beside the verifies of layers l+1, ...; the step ends with a join
+        # the verify of every layer in order on the main stream; the accept and flush
+        # of layer l (needed only by layer l's next verify, one step later) run on one
+        # of two side streams beside the verifies of layers l+1, ...; the step ends
+        # with a join
         main = torch.cuda.current_stream()
         for l in range(L):
             blk = pools[l][j % DRAFT_POOL] if blocks is None else blocks[l]
+            acc = acc_dev[l][j] if accs is None else accs[l]
             layers[l].verify(blk["q"], blk["k"], blk["v"], blk["g"], blk["beta"], outs[l])
-            layers[l].accept(acc_dev[l][j] if accs is None else accs[l])
+            side = sides[l % len(sides)]
             fork[l].record(main)
             side.wait_event(fork[l])
             with torch.cuda.stream(side):
+                layers[l].accept(acc)
                 layers[l].flush(force=False)
-        main.wait_stream(side)
+        for side in sides:
+            main.wait_stream(side)
 
     def enqueue_step(j, events=None):
         if overlap:
@@ -501,9 +505,9 @@ def main():
             cpu = {"value": round(el * 1e6 / n, 3), "unit": "us/layer", "cores": threads,
                    "kind": "oracle", "sample": f"layer 0, B={B}, {n} consecutive layer-steps "
                                                f"(~{args.cpu_seconds:.0f} s of fp64 C on host cores)"}
-        steps_desc = {"overlap": "per layer gdn_replay_verify + gdn_replay_accept on the main stream; "
-                                 "gdn_replay_flush of each layer on a side stream beside the following "
-                                 "layers' verifies (a layer's flush is needed only by its next verify); "
+        steps_desc = {"overlap": "per layer gdn_replay_verify on the main stream; gdn_replay_accept + "
+                                 "gdn_replay_flush of each layer on one of two side streams beside the following "
+                                 "layers' verifies (they are needed only by that layer's next verify); "
                                  "the step ends with a join",
                       "fused": "gdn_replay_verify_fold + gdn_replay_accept_fold per layer (flush folded "
                                "into the next verify)",
