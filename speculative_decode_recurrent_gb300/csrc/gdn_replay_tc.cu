@@ -192,31 +192,41 @@ __device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
 // 16 KB buffers in quarters of 32 columns once the token work is done.
 //
 // Shared-memory plan (bytes from the 1024-aligned base), NPA = round16(CMAX + 16):
-//   [0, 2 SUBK)          [K;Q] rows, bf16, 2 sub-tiles (d_k halves) of NPA rows x 128 B
-//   [OFF_V, +2 SUBV)     value rows, bf16, 2 sub-tiles of CMAX rows x 128 B
+//   [0, 2 SUBV)          value rows, bf16, 2 sub-tiles (d_k halves) of CMAX rows x 128 B
+//   [OFF_K, +2 SUBK)     [K;Q] rows, bf16, 2 sub-tiles of NPA rows x 128 B
 //   [OFF_A, +CMAX^2 4)   A, fp32, row-major [CMAX][CMAX]
 //   [OFF_M, +16 CMAX 4)  M, fp32, row-major [16][CMAX]
-//   [OFF_W, +8K)         W beta gamma and W beta as 2 + 2 bf16 tiles [16][64]; later
-//                        qe as fp32 [16][128] (4 sub-tiles of 16 rows x 128 B)
+//   [OFF_A, +8K)         after the back substitution: W beta gamma and W beta as 2 + 2
+//                        bf16 tiles [16][64]
 //   [0, 32K)             after the token contractions: two checkpoint quarter buffers
+//   [OFF_QE, +8K)        then qe as fp32 [16][128] (4 sub-tiles of 16 rows x 128 B)
 //   [OFF_S, ...)         8 mbarriers, TMEM slot, flag, then G (hi, lo), beta, gamma
 // An M = 128 operand starting in the [K;Q] tile reads on past its NPA rows; those
-// rows only feed accumulator lanes that are never read.
-constexpr int kTmemColsEq = 128;
+// rows only feed accumulator lanes that are never read.  [K;Q] K^T is formed as two
+// MMAs: lanes 0..63 get rows 0..63 and the first columns, and, from an operand that
+// starts 64 rows before the tile, lanes 64..127 get rows 0..63 and the remaining
+// columns, so all four warps build coefficients.
 template <int CMAX> struct EqPlan {
     static constexpr int NPA = (CMAX + 16 + 15) & ~15;
     static constexpr int SUBK = NPA * 128;
     static constexpr int SUBV = CMAX * 128;
-    static constexpr int OFF_V = 2 * SUBK;
-    static constexpr int OFF_A = OFF_V + 2 * SUBV;
+    static constexpr int OFF_K = 2 * SUBV;
+    static constexpr int OFF_A = OFF_K + 2 * SUBK;
     static constexpr int OFF_M = OFF_A + CMAX * CMAX * 4;
-    static constexpr int OFF_W = (OFF_M + 16 * CMAX * 4 + 1023) & ~1023;
-    static constexpr int OFF_S = OFF_W + 8192;
+    static constexpr int OFF_W = OFF_A;                       // over A and M, once they are read
+    static constexpr int OFF_QE = 32768;                      // past the two quarter buffers
+    static constexpr int A_END = OFF_M + 16 * CMAX * 4;
+    static constexpr int OFF_S = ((A_END > OFF_QE + 8192 ? A_END : OFF_QE + 8192) + 127) & ~127;
     static constexpr int BYTES = OFF_S + 128 + 16 * CMAX;
-    static_assert(OFF_W >= 32768, "the quarter buffers must not reach the qe tile");
-    static_assert(SUBK + 16384 <= BYTES, "M = 128 operand reads stay inside the allocation");
+    // TMEM: K.K in [0, CMAX) (then ve, O over it), qe^T in [CMAX, CMAX + 16)
+    static constexpr int TMEM_COLS = CMAX + 16 <= 64 ? 64 : 128;
+    static constexpr int BLOCKS_PER_SM = CMAX + 16 <= 64 ? 5 : 3;
+    static_assert(OFF_W % 1024 == 0 && OFF_W + 8192 <= A_END, "W tiles over A and M");
+    static_assert(OFF_QE >= 32768 && OFF_QE + 8192 <= OFF_S, "qe tile past the quarter buffers");
+    static_assert(OFF_K + SUBK + 16384 <= BYTES, "M = 128 operand reads stay inside the allocation");
+    static_assert(OFF_K >= 8192, "an operand may start 64 rows before the [K;Q] tile");
     static_assert(CMAX % 16 == 0 && CMAX <= 64, "token columns: at most two per lane");
-    static_assert((SUBK % 1024) == 0 && (OFF_V % 1024) == 0 && (SUBV % 1024) == 0, "swizzle atoms");
+    static_assert((SUBK % 1024) == 0 && (OFF_K % 1024) == 0 && (SUBV % 1024) == 0, "swizzle atoms");
 };
 
 // MN-major operand, 128-byte swizzle: 64-element atoms along M/N `lbo` bytes apart,
@@ -229,7 +239,7 @@ __device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t addr, uint32_t lbo) {
 constexpr uint32_t kIdescMnMajorA = 1u << 15;
 
 template <int CMAX>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, EqPlan<CMAX>::BLOCKS_PER_SM)
 verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
 {
     using P = EqPlan<CMAX>;
@@ -241,12 +251,12 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
         if (tid == 0) atomicOr(a.status, kStatusTimeout);
         return;
     }
-    uint8_t *sKQ = smem_raw;
-    uint8_t *sV = smem_raw + P::OFF_V;
+    uint8_t *sV = smem_raw;
+    uint8_t *sKQ = smem_raw + P::OFF_K;
     float *sAm = reinterpret_cast<float *>(smem_raw + P::OFF_A);
     float *sMm = reinterpret_cast<float *>(smem_raw + P::OFF_M);
     uint8_t *sW = smem_raw + P::OFF_W;
-    uint8_t *sQe = sW;
+    uint8_t *sQe = smem_raw + P::OFF_QE;
     uint8_t *sm = smem_raw + P::OFF_S;
     // 0, 1: checkpoint buffers (TMA); 2: K.K; 3: qe, ve; 4..7: checkpoint quarter MMAs
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm);
@@ -256,7 +266,7 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     float *sGl = sGh + CMAX;
     float *sBeta = sGl + CMAX;
     float *sGam = sBeta + CMAX;
-    constexpr int COL_Q = CMAX, COL_V = CMAX + 16, COL_O = CMAX + 32;   // TMEM columns
+    constexpr int COL_Q = CMAX, COL_V = 0, COL_O = 16;           // TMEM columns (ve, O over K.K)
 
     if (tid == 0) {                                               // prologue: no global memory
 #pragma unroll
@@ -264,7 +274,7 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
         *flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0) tmem_alloc(tmem_slot, kTmemColsEq);
+    if (warp == 0) tmem_alloc(tmem_slot, P::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -289,7 +299,7 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     auto finish = [&]() {
         tc_fence_before();
         __syncthreads();
-        if (warp == 0) tmem_dealloc(tmem, kTmemColsEq);
+        if (warp == 0) tmem_dealloc(tmem, P::TMEM_COLS);
         if (waiter) pdl_wait();
     };
     if (bad || other_class) {                                     // uniform across the CTA
@@ -299,6 +309,10 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     }
     const int C = len + T;
     const int CP = round16(C);
+    // [K;Q] K^T in two column ranges (rows 0..63 also in lanes 64..127) when every row
+    // of [K;Q] fits in 64 lanes; else one MMA over all columns
+    constexpr bool kSplitKK = CMAX + 16 <= 64;
+    const int ca = !kSplitKK ? CP : CP == 16 ? 16 : ((CP / 2 + 15) & ~15);   // columns of the first MMA
     const size_t unit = static_cast<size_t>(slot) * H + h;
     const int ytile = static_cast<int>(unit) * 128;
 
@@ -415,12 +429,19 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
         tc_fence_after();
 #pragma unroll
         for (int q = 0; q < 4; ++q) prefetch_tile_l2(&tm_state, q * 32, ytile);
-        const uint32_t idK = idesc_mn(1, 128, CP);
-        const uint64_t dkq = desc_sw128(kq0);
+        const uint64_t dkq = desc_sw128(kq0), dkq_up = desc_sw128(kq0 - 8192);
+        const uint32_t idA = idesc_mn(1, 128, ca), idB = idesc_mn(1, 128, CP - ca);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
+        for (int ks = 0; ks < 8; ++ks) {                          // lanes 0..127 = rows, columns [0, ca)
             const uint64_t d = desc_add(dkq, (ks >> 2) * P::SUBK + (ks & 3) * 32);
-            mma_bf16(tmem, d, d, idK, ks > 0);
+            mma_bf16(tmem, d, d, idA, ks > 0);
+        }
+        if (kSplitKK && CP > ca) {                                // lanes 64..127 = rows, columns [ca, CP)
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t off = (ks >> 2) * P::SUBK + (ks & 3) * 32;
+                mma_bf16(tmem + ca, desc_add(dkq_up, off), desc_add(dkq, off + ca * 128), idB, ks > 0);
+            }
         }
         mma_commit(&bar[2]);
     }
@@ -444,22 +465,26 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     }
     tc_fence_after();
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    // ---- coefficient rows: TMEM lane r = row r of [K;Q]; key rows t < C give
-    //      A[t][s] = beta_t e^{G_t-G_s} (k_t.k_s) (s < t), query rows C + t2 give
-    //      M[t2][s] = e^{G_p-G_s} (q_t2.k_s) (s <= p); rows t2 >= T of M are zero
-    if (warp * 32 < C + 16) {                                     // warp-uniform: the loads are collective
-        const bool is_q = tid >= C;
-        const int t2 = tid - C;
-        const bool writes = tid < C + 16;
-        const bool live = tid < C + T;
-        const int p = !live ? C - 1 : is_q ? len + t2 : tid;
+    // ---- coefficient rows: row r of [K;Q] (TMEM lane r for columns [0, ca), lane
+    //      64 + r for [ca, CP)); key rows t < C give A[t][s] = beta_t e^{G_t-G_s} (k_t.k_s)
+    //      (s < t), query rows C + t2 give M[t2][s] = e^{G_p-G_s} (q_t2.k_s) (s <= p);
+    //      rows t2 >= T of M are zero; warps 0-1 write columns [0, ca), warps 2-3 the rest
+    const int row = kSplitKK ? (tid & 63) : tid;
+    if ((kSplitKK ? (warp & 1) : warp) * 32 < C + 16) {           // warp-uniform: the loads are collective
+        const bool is_q = row >= C;
+        const int t2 = row - C;
+        const bool writes = row < C + 16;
+        const bool live = row < C + T;
+        const int p = !live ? C - 1 : is_q ? len + t2 : row;
         const float gh = sGh[p], gl = sGl[p];
         const float scl = is_q ? 1.f : sBeta[p];
-        const int lim = !live ? 0 : is_q ? min(p + 1, C) : tid;
-        float *dst = is_q ? sMm + (writes ? t2 : 0) * CMAX : sAm + tid * CMAX;
+        const int lim = !live ? 0 : is_q ? min(p + 1, C) : row;
+        float *dst = is_q ? sMm + (writes ? t2 : 0) * CMAX : sAm + row * CMAX;
+        const int cbeg = (!kSplitKK || warp < 2) ? 0 : ca, cend = (!kSplitKK || warp >= 2) ? CMAX : ca;
 #pragma unroll
         for (int cb = 0; cb < CMAX / 16; ++cb) {
             const int c0 = cb * 16;
+            if (c0 < cbeg || c0 >= cend) continue;                // warp-uniform
             float kq[16];
             if (c0 < CP) {
                 tmem_ld16(lane_base + c0, kq);
@@ -488,6 +513,7 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
             }
         }
     }
+    tc_fence_before();                                            // K.K columns are reused by ve and O
     __syncthreads();
     // ---- W = M (I + A)^{-1}: warp w holds draft rows 4w .. 4w + 3, lane l token columns
     //      l and l + 32; column s is final once every s' > s has been subtracted
@@ -510,6 +536,7 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
             x1[i] = fmaf(-w, a1, x1[i]);
         }
     }
+    __syncthreads();                                              // A, M no longer read: W goes over them
     // ---- W beta gamma and W beta as K-major [16][64] tiles, each the sum of two bf16
     //      terms (relative error 2^-16, far below that of the tf32 checkpoint product)
 #pragma unroll
