@@ -694,9 +694,9 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
 // buffer is then empty) and stages it at buffer slot 0.
 //
 // Shared-memory plan (bytes from the 1024-aligned base), Lp = CMAX:
-//   [0, 2 SUBK)            key rows, bf16, 2 sub-tiles of CMAX rows x 128 B
 //   [OFF_AT, +Lp^2 4)      A^T, fp32 (row s holds column s of A)
 //   [OFF_TI, +Lp^2 4)      Tinv, fp32 row-major; then the block scratch
+//   [OFF_K, +2 SUBK)       key rows, bf16, 2 sub-tiles of CMAX rows x 128 B
 //   [0, 32K)               after E' is formed: E'^T as two bf16 tiles [128][64]
 //   [OFF_V, +2 SUBV)       value rows, bf16
 //   [OFF_KF, +4 KFSUB)     key rows, fp32, 4 sub-tiles of CMAX rows x 128 B (S0 K^T);
@@ -708,20 +708,23 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
 //   [OFF_SC, ...)          mbarriers, TMEM slot, flags, G (hi, lo), beta, gamma, D, list
 template <int CMAX> struct FoldPlan {
     static constexpr int SUBK = CMAX * 128;
-    static constexpr int OFF_AT = 2 * SUBK;
+    static constexpr int OFF_AT = 0;
     static constexpr int OFF_TI = OFF_AT + CMAX * CMAX * 4;
     static constexpr int OFF_Y = OFF_TI + CMAX * CMAX * 4;    // Tinv block scratch
     static constexpr int Y_END = OFF_Y + (CMAX / 16 - 1) * 1024;
-    static constexpr int OFF_V = ((Y_END > 32768 ? Y_END : 32768) + 1023) & ~1023;
+    static constexpr int OFF_K = (Y_END + 1023) & ~1023;      // >= 8 KB: an operand may start 64 rows before
+    static constexpr int K_END = OFF_K + 2 * SUBK;
+    static constexpr int OFF_V = ((K_END > 32768 ? K_END : 32768) + 1023) & ~1023;
     static constexpr int SUBV = CMAX * 128;
     static constexpr int OFF_KF = OFF_V + 2 * SUBV;
     static constexpr int KFSUB = CMAX * 128;
     static constexpr int OFF_Q = OFF_KF + 4 * KFSUB;
     static constexpr int OFF_SC = OFF_Q + 32768;
     static constexpr int LIST = 512;
-    static constexpr int BYTES = OFF_SC + 128 + 20 * CMAX + 4 * LIST + 256;
+    static constexpr int BYTES = OFF_SC + 160 + 20 * CMAX + 4 * LIST + 256;
     static_assert(CMAX == 48 || CMAX == 64, "token blocks");
-    static_assert(SUBK + 16384 <= OFF_SC, "M = 128 operand reads stay inside the allocation");
+    static_assert(OFF_K + SUBK + 16384 <= OFF_SC, "M = 128 operand reads stay inside the allocation");
+    static_assert(OFF_K >= 8192 && K_END <= OFF_V, "64 rows of room before the keys; keys below the values");
     static_assert(2 * CMAX * 128 <= 4 * KFSUB, "F over the fp32 key tile");
     static_assert(4 * KFSUB >= 22528, "draft tiles in the fp32 key region");
     static_assert(2 * SUBV >= 8192, "draft qe tile over the value rows");
@@ -744,7 +747,7 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
         if (tid == 0) atomicOr(a.status, kStatusTimeout);
         return;
     }
-    uint8_t *sK = smem_raw;
+    uint8_t *sK = smem_raw + P::OFF_K;
     float *sAt = reinterpret_cast<float *>(smem_raw + P::OFF_AT);
     float *sTi = reinterpret_cast<float *>(smem_raw + P::OFF_TI);
     uint8_t *sEt = smem_raw;                                      // 2 x 16 KB
@@ -760,11 +763,11 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
     // 0: K.K; 1: E^T; 2, 3: checkpoint buffers; 4..7: S0 K^T quarters; 8: fold;
     // 9..11: draft (K_d K_d^T, qe/ve, S_L qe^T)
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + 96);
-    int *flag = reinterpret_cast<int *>(sm + 100);
-    int *n_list = reinterpret_cast<int *>(sm + 104);
-    int *warp_cnt = reinterpret_cast<int *>(sm + 112);             // [4]
-    float *sGh = reinterpret_cast<float *>(sm + 128);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + 128);
+    int *flag = reinterpret_cast<int *>(sm + 132);
+    int *n_list = reinterpret_cast<int *>(sm + 136);
+    int *warp_cnt = reinterpret_cast<int *>(sm + 144);             // [4]
+    float *sGh = reinterpret_cast<float *>(sm + 160);
     float *sGl = sGh + CMAX;
     float *sBeta = sGl + CMAX;
     float *sGam = sBeta + CMAX;
@@ -781,14 +784,13 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
         for (int i = 0; i < 12; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
     }
-    if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
-    tc_fence_before();
     __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     pdl_wait();
     pdl_release();
+    // TMEM is taken at the first item only: a CTA without one leaves the columns to
+    // the kernels running beside this launch
+    uint32_t tmem = 0, lane_base = 0;
+    bool have_tmem = false;
     const uint32_t k0 = saddr(sK), f0 = saddr(sF), kf0 = saddr(sKf), buf0 = saddr(sBuf), r0 = saddr(sR),
                    e0 = saddr(sEt), v0 = saddr(sV);
     // base descriptors (issue sequences add constant offsets)
@@ -826,6 +828,15 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
         }
         const int n_items = *n_list * H;
         for (int w = blockIdx.x; w < n_items && alive; w += gridDim.x, ++it) {
+            if (!have_tmem) {                                     // uniform across the CTA
+                if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
+                tc_fence_before();
+                __syncthreads();
+                tc_fence_after();
+                tmem = *tmem_slot;
+                lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+                have_tmem = true;
+            }
             const uint32_t ph = it & 1u;
             const int b = list[w / H], h = w % H;
             const int slot = a.state_idx ? a.state_idx[b] : b;
@@ -946,13 +957,25 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                 tma_load_2d(sBuf + bi * 16384, &tm_state, q * 32, ytile, &bar[2 + bi]);
                 ++loads[bi];
             };
-            if (tid == 0) {                                       // K K^T; quarters 0 and 1
+            // K K^T in two column ranges: lanes 0..63 hold rows 0..63 for columns [0, ca),
+            // and, from an operand starting 64 rows before the key tile, lanes 64..127
+            // hold rows 0..63 for columns [ca, Lp); all four warps then build A^T
+            const int ca = Lp == 16 ? 16 : ((Lp / 2 + 15) & ~15);
+            if (tid == 0) {                                       // K K^T
                 tc_fence_after();
-                const uint32_t idK = idesc_mn(1, 128, Lp);
+                const uint32_t idA = idesc_mn(1, 128, ca), idB = idesc_mn(1, 128, Lp - ca);
+                const uint64_t dKup = desc_sw128(k0 - 8192);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint64_t d = desc_add(dK, (ks >> 2) * P::SUBK + (ks & 3) * 32);
-                    mma_bf16(tmem + COL_KK, d, d, idK, ks > 0);
+                    mma_bf16(tmem + COL_KK, d, d, idA, ks > 0);
+                }
+                if (Lp > ca) {
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t off = (ks >> 2) * P::SUBK + (ks & 3) * 32;
+                        mma_bf16(tmem + COL_KK + ca, desc_add(dKup, off), desc_add(dK, off + ca * 128), idB, ks > 0);
+                    }
                 }
                 mma_commit(&bar[0]);
             }
@@ -976,13 +999,16 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                 break;
             }
             tc_fence_after();
-            // ---- A^T: thread t writes column t of A (row t of A^T): A[t][s] for s < t
-            if (warp * 32 < CMAX) {                               // warp-uniform: collective loads
-                const int t = tid;
+            // ---- A^T: thread t writes column t of A (row t of A^T): A[t][s] for s < t;
+            //      warps 0-1 columns s in [0, ca), warps 2-3 the rest (token t = tid & 63)
+            if ((warp & 1) * 32 < CMAX) {                         // warp-uniform: collective loads
+                const int t = tid & 63;
                 const float gh = t < L ? sGh[t] : 0.f, gl = t < L ? sGl[t] : 0.f, bt = t < L ? sBeta[t] : 0.f;
+                const int cbeg = warp < 2 ? 0 : ca, cend = warp < 2 ? ca : CMAX;
 #pragma unroll
                 for (int cb = 0; cb < CMAX / 16; ++cb) {
                     const int c0 = cb * 16;
+                    if (c0 < cbeg || c0 >= cend) continue;        // warp-uniform
                     float kk[16];
                     if (c0 < Lp) {
                         tmem_ld16(lane_base + COL_KK + c0, kk);
@@ -1474,7 +1500,7 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+    if (have_tmem && warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ------------------------------------------------------------------ host side
