@@ -43,7 +43,10 @@ ACCEPT_PERIOD = 16      # distinct accepted-count patterns, cycled over steps
 FALLBACK_HBM_GBS = 6800.0
 # dram read+write bytes per verify launch from the ncu capture summarised in
 # profiles/; valid only for the kernel source whose hash is recorded with it.
-NCU_TRAFFIC = {}        # {(step mode, source_sha1): bytes_per_launch}
+NCU_TRAFFIC = {         # {(step mode, source_sha1): dram read + write bytes per launch}
+    ("three_call", "e953632af3595891bb5a47069c23f7c6e8171bc3"): 43.31e6,   # verify_eq_kernel, launch list of profiles/
+    ("fused", "e953632af3595891bb5a47069c23f7c6e8171bc3"): 46.23e6,        # fold launch 14.05 MB + verify launch 32.18 MB
+}
 
 
 def parse():
