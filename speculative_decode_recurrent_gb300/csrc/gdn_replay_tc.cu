@@ -39,6 +39,9 @@ namespace {
 constexpr int kThreads = 128;               // one thread per state row / TMEM lane
 constexpr uint32_t kWaitLimit = 1u << 21;   // mbarrier polls before giving up
 constexpr int kTmemCols = 256;
+// Registers of a fold thread: one fold CTA (and its 256 TMEM columns) leaves room on
+// its SM for three verify CTAs (3 x 128 x 96 + 128 x 224 = 65536).
+constexpr int kFoldRegs = 224;
 
 // ------------------------------------------------------------ PTX wrappers
 __device__ __forceinline__ uint32_t saddr(const void *p) {
@@ -720,8 +723,7 @@ template <int CMAX> struct FoldPlan {
     static constexpr int KFSUB = CMAX * 128;
     static constexpr int OFF_Q = OFF_KF + 4 * KFSUB;
     static constexpr int OFF_SC = OFF_Q + 32768;
-    static constexpr int LIST = 512;
-    static constexpr int BYTES = OFF_SC + 160 + 20 * CMAX + 4 * LIST + 256;
+    static constexpr int BYTES = OFF_SC + 160 + 20 * CMAX + 256;
     static_assert(CMAX == 48 || CMAX == 64, "token blocks");
     static_assert(OFF_K + SUBK + 16384 <= OFF_SC, "M = 128 operand reads stay inside the allocation");
     static_assert(OFF_K >= 8192 && K_END <= OFF_V, "64 rows of room before the keys; keys below the values");
@@ -735,7 +737,7 @@ template <int CMAX> struct FoldPlan {
 };
 
 template <int CMAX, bool DRAFT>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __maxnreg__(kFoldRegs)
 fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
 {
     using P = FoldPlan<CMAX>;
@@ -765,15 +767,13 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + 128);
     int *flag = reinterpret_cast<int *>(sm + 132);
-    int *n_list = reinterpret_cast<int *>(sm + 136);
-    int *warp_cnt = reinterpret_cast<int *>(sm + 144);             // [4]
+    uint32_t *fmask = reinterpret_cast<uint32_t *>(sm + 144);     // [4]: folding sequences of a chunk
     float *sGh = reinterpret_cast<float *>(sm + 160);
     float *sGl = sGh + CMAX;
     float *sBeta = sGl + CMAX;
     float *sGam = sBeta + CMAX;
     float *sD = sGam + CMAX;
-    int *list = reinterpret_cast<int *>(sD + CMAX);
-    float *dGh = reinterpret_cast<float *>(list + P::LIST);      // draft: G (hi, lo), beta, gamma
+    float *dGh = sD + CMAX;      // draft: G (hi, lo), beta, gamma
     float *dGl = dGh + 16;
     float *dBeta = dGl + 16;
     float *dGam = dBeta + 16;
@@ -800,33 +800,25 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
 
     uint32_t it = 0;                                              // items done by this CTA
     bool alive = true;
-    for (int b0 = 0; b0 < a.B && alive; b0 += P::LIST) {
-        // the list must be identical in every CTA: compact in sequence order with
-        // ballots and a prefix over the four warps (no atomics)
-        if (tid == 0) *n_list = 0;
-        __syncthreads();
-        const int bend = min(b0 + P::LIST, a.B);
-        for (int g0 = b0; g0 < bend; g0 += kThreads) {
-            const int bb = g0 + tid;
-            bool f = false;
-            if (bb < bend) {
-                const int sl = a.state_idx ? a.state_idx[bb] : bb;
-                if (sl >= 0 && sl < a.n_slot) {                     // others: reported by the length kernel
-                    const int ln = a.buf_len[sl];
-                    f = ln >= 0 && ln <= cap && (ln >= a.threshold || (a.force && ln > 0));
-                }
+    for (int b0 = 0; b0 < a.B && alive; b0 += kThreads) {
+        // the folding sequences of this chunk of 128, identical in every CTA: one
+        // ballot per warp; item n of the chunk is the n-th set bit over the four masks
+        const int bb = b0 + tid;
+        bool f = false;
+        if (bb < a.B) {
+            const int sl = a.state_idx ? a.state_idx[bb] : bb;
+            if (sl >= 0 && sl < a.n_slot) {                         // others: reported by the length kernel
+                const int ln = a.buf_len[sl];
+                f = ln >= 0 && ln <= cap && (ln >= a.threshold || (a.force && ln > 0));
             }
-            const unsigned m = __ballot_sync(0xffffffffu, f);
-            if (lane == 0) warp_cnt[warp] = __popc(m);
-            __syncthreads();
-            int base = *n_list;
-            for (int w2 = 0; w2 < warp; ++w2) base += warp_cnt[w2];
-            if (f) list[base + __popc(m & ((1u << lane) - 1u))] = bb;
-            __syncthreads();
-            if (tid == 0) *n_list += warp_cnt[0] + warp_cnt[1] + warp_cnt[2] + warp_cnt[3];
-            __syncthreads();
         }
-        const int n_items = *n_list * H;
+        const uint32_t m = __ballot_sync(0xffffffffu, f);
+        __syncthreads();                                          // the previous chunk's masks are read
+        if (lane == 0) fmask[warp] = m;
+        __syncthreads();
+        const uint32_t m0 = fmask[0], m1 = fmask[1], m2 = fmask[2], m3 = fmask[3];
+        const int c1 = __popc(m0), c2 = c1 + __popc(m1), c3 = c2 + __popc(m2);
+        const int n_items = (c3 + __popc(m3)) * H;
         for (int w = blockIdx.x; w < n_items && alive; w += gridDim.x, ++it) {
             if (!have_tmem) {                                     // uniform across the CTA
                 if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
@@ -838,7 +830,11 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                 have_tmem = true;
             }
             const uint32_t ph = it & 1u;
-            const int b = list[w / H], h = w % H;
+            const int n = w / H, h = w % H;
+            const int wi = n < c1 ? 0 : n < c2 ? 1 : n < c3 ? 2 : 3;
+            const int b = b0 + wi * 32 +
+                          static_cast<int>(__fns(wi == 0 ? m0 : wi == 1 ? m1 : wi == 2 ? m2 : m3, 0u,
+                                                 n - (wi == 0 ? 0 : wi == 1 ? c1 : wi == 2 ? c2 : c3) + 1));
             const int slot = a.state_idx ? a.state_idx[b] : b;
             const int L = a.buf_len[slot];
             const int Lp = round16(L);
