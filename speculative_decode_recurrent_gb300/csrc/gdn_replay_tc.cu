@@ -298,7 +298,10 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     if (slot < 0 || slot >= a.n_slot) bad = GDN_STATUS_BAD_SLOT;
     else if (len < 0 || len > cap) bad = GDN_STATUS_BAD_LEN;
     else if (!other_class && len + T > cap) bad = GDN_STATUS_NO_ROOM;
-    pdl_release();                                                // every length of this CTA is read
+    // No early launch_dependents here: the next launch starts as these CTAs exit, so
+    // the block scheduler spreads its CTAs evenly over the SMs (CTAs let in early
+    // fill the SMs that happen to finish first, up to five on one SM, and the most
+    // crowded SM then sets the length of that launch).
     auto finish = [&]() {
         tc_fence_before();
         __syncthreads();
