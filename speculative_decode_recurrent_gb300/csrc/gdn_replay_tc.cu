@@ -298,10 +298,10 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     if (slot < 0 || slot >= a.n_slot) bad = GDN_STATUS_BAD_SLOT;
     else if (len < 0 || len > cap) bad = GDN_STATUS_BAD_LEN;
     else if (!other_class && len + T > cap) bad = GDN_STATUS_NO_ROOM;
-    // No early launch_dependents here: the next launch starts as these CTAs exit, so
-    // the block scheduler spreads its CTAs evenly over the SMs (CTAs let in early
-    // fill the SMs that happen to finish first, up to five on one SM, and the most
-    // crowded SM then sets the length of that launch).
+    // launch_dependents comes only before the epilogue: the next launch then starts
+    // as these CTAs finish, and the block scheduler spreads its CTAs evenly over the
+    // SMs (CTAs let in early fill the SMs that happen to finish first, up to five on
+    // one SM, and the most crowded SM then sets the length of that launch).
     auto finish = [&]() {
         tc_fence_before();
         __syncthreads();
@@ -661,6 +661,7 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
         finish();
         return;
     }
+    pdl_release();                                                // the outputs are all that is left
     tc_fence_after();
     {
         float o[16], ve[16];
