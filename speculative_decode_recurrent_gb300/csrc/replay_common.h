@@ -31,7 +31,7 @@ struct ReplayArgs {
 // programmatic stream serialisation and waits (griddepcontrol.wait) before its first
 // read of global memory another kernel may have written.  All but the verify kernel
 // then let the next kernel on the stream start its launch and prologue
-// (launch_dependents); the verify kernel's successor launches as its CTAs exit.
+// (launch_dependents); the verify kernel does so only before its epilogue.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
