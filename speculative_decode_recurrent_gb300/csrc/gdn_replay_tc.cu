@@ -291,6 +291,31 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     const bool waiter = split && blockIdx.x == 0 && blockIdx.y == 0;
     if (!split) pdl_wait();
 
+    // ---- the draft rows first: their addresses do not depend on the buffer length,
+    //      so they are in flight while the slot and the length are read.  Vector i of
+    //      a thread is row (tid >> 4) + 8 (i & 1) of the draft keys (i < 2), queries
+    //      (i < 4) or values, 16-byte column tid & 15.
+    const size_t drow0 = (static_cast<size_t>(b) * T * H + h) * 128;
+    const size_t dstride = static_cast<size_t>(H) * 128;
+    const __nv_bfloat16 *dk = reinterpret_cast<const __nv_bfloat16 *>(a.k) + drow0;
+    const __nv_bfloat16 *dq = reinterpret_cast<const __nv_bfloat16 *>(a.q) + drow0;
+    const __nv_bfloat16 *dv = reinterpret_cast<const __nv_bfloat16 *>(a.v) + drow0;
+    const int dj = tid >> 4, dc = tid & 15;                       // draft row (+ 8), column vector
+    uint4 draft[6];
+#pragma unroll
+    for (int i = 0; i < 6; ++i) {
+        const int j = dj + 8 * (i & 1);
+        const __nv_bfloat16 *src = i < 2 ? dk : i < 4 ? dq : dv;
+        draft[i] = j < T ? __ldg(reinterpret_cast<const uint4 *>(src + static_cast<size_t>(j) * dstride) + dc)
+                         : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float dg = 0.f, db = 0.f;                                     // warp 0: draft token `lane`
+    if (warp == 0 && lane < T) {
+        const size_t gi = (static_cast<size_t>(b) * T + lane) * H + h;
+        dg = a.g[gi];
+        db = a.beta[gi];
+    }
+
     const int slot = a.state_idx ? a.state_idx[b] : b;
     const int len = (slot >= 0 && slot < a.n_slot) ? a.buf_len[slot] : 0;
     const bool other_class = split && len >= a.threshold && len <= cap;   // the fold launch's unit
@@ -322,40 +347,21 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     const size_t unit = static_cast<size_t>(slot) * H + h;
     const int ytile = static_cast<int>(unit) * 128;
 
-    // ---- every global load of this unit, issued back to back (the checkpoint, needed
-    //      last, is prefetched into L2 once these rows are in, so they come first)
+    // ---- the buffered rows (keys, values, gates) of this unit
     const __nv_bfloat16 *bk = reinterpret_cast<const __nv_bfloat16 *>(a.buf_k) + unit * cap * 128;
     const __nv_bfloat16 *bv = reinterpret_cast<const __nv_bfloat16 *>(a.buf_v) + unit * cap * 128;
-    const size_t drow0 = (static_cast<size_t>(b) * T * H + h) * 128;
-    const size_t dstride = static_cast<size_t>(H) * 128;
-    const __nv_bfloat16 *dk = reinterpret_cast<const __nv_bfloat16 *>(a.k) + drow0;
-    const __nv_bfloat16 *dq = reinterpret_cast<const __nv_bfloat16 *>(a.q) + drow0;
-    const __nv_bfloat16 *dv = reinterpret_cast<const __nv_bfloat16 *>(a.v) + drow0;
     __nv_bfloat16 *wk = reinterpret_cast<__nv_bfloat16 *>(a.buf_k) + (unit * cap + len) * 128;
     __nv_bfloat16 *wv = reinterpret_cast<__nv_bfloat16 *>(a.buf_v) + (unit * cap + len) * 128;
-    constexpr int NV = P::NPA * 16 / kThreads;                   // 16-byte vectors of [K;Q] per thread
-    uint4 raw[NV];
+    constexpr int NB = 4;                                         // rows 0 .. 31 in registers (T = 16:
+    uint4 bkr[NB], bvr[NB];                                       // every buffered row); the rest below
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
-        raw[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (r < C + T) {
-            const __nv_bfloat16 *src = r < len ? bk + static_cast<size_t>(r) * 128
-                                     : r < C   ? dk + static_cast<size_t>(r - len) * dstride
-                                               : dq + static_cast<size_t>(r - C) * dstride;
-            raw[i] = __ldg(reinterpret_cast<const uint4 *>(src) + c);
-        }
-    }
-    constexpr int NVV = CMAX * 16 / kThreads;
-    uint4 vload[NVV];
-#pragma unroll
-    for (int i = 0; i < NVV; ++i) {
-        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
-        vload[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (r < C) {
-            const __nv_bfloat16 *src = r < len ? bv + static_cast<size_t>(r) * 128
-                                               : dv + static_cast<size_t>(r - len) * dstride;
-            vload[i] = __ldg(reinterpret_cast<const uint4 *>(src) + c);
+    for (int i = 0; i < NB; ++i) {
+        const int r = dj + 8 * i;
+        bkr[i] = make_uint4(0u, 0u, 0u, 0u);
+        bvr[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < len) {
+            bkr[i] = __ldg(reinterpret_cast<const uint4 *>(bk + static_cast<size_t>(r) * 128) + dc);
+            bvr[i] = __ldg(reinterpret_cast<const uint4 *>(bv + static_cast<size_t>(r) * 128) + dc);
         }
     }
     float gq[2] = {0.f, 0.f}, bq[2] = {0.f, 0.f};
@@ -363,31 +369,52 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int t = lane + 32 * i;
-            if (t < C) {
-                if (t < len) {
-                    gq[i] = a.buf_g[unit * cap + t];
-                    bq[i] = a.buf_beta[unit * cap + t];
-                } else {
-                    const size_t gi = (static_cast<size_t>(b) * T + (t - len)) * H + h;
-                    gq[i] = a.g[gi];
-                    bq[i] = a.beta[gi];
-                }
+            if (t < len) {
+                gq[i] = a.buf_g[unit * cap + t];
+                bq[i] = a.buf_beta[unit * cap + t];
+            }
+            // draft token t - len sits in lane t - len (every lane takes part)
+            const int src = t >= len && t < C ? t - len : 0;
+            const float g2 = __shfl_sync(0xffffffffu, dg, src), b2 = __shfl_sync(0xffffffffu, db, src);
+            if (t >= len && t < C) {
+                gq[i] = g2;
+                bq[i] = b2;
             }
         }
     }
-    // ---- rows into the swizzled bf16 tiles (zeros past the last token); the draft
-    //      keys and values into the buffer (slots len .. len + T - 1, never read here)
+    // ---- rows into the swizzled bf16 tiles: [K;Q] = buffered keys, draft keys, draft
+    //      queries, then zeros; V = buffered values, draft values, then zeros.  The
+    //      draft keys and values also go to the buffer (slots len .. len + T - 1).
+    auto kq_at = [&](int r, int c) { return reinterpret_cast<uint4 *>(sKQ + (c >> 3) * P::SUBK + sw128(r, c & 7)); };
+    auto v_at = [&](int r, int c) { return reinterpret_cast<uint4 *>(sV + (c >> 3) * P::SUBV + sw128(r, c & 7)); };
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
-        *reinterpret_cast<uint4 *>(sKQ + (c >> 3) * P::SUBK + sw128(r, c & 7)) = raw[i];
-        if (r >= len && r < C) reinterpret_cast<uint4 *>(wk + static_cast<size_t>(r - len) * 128)[c] = raw[i];
+    for (int i = 0; i < NB; ++i) {
+        const int r = dj + 8 * i;
+        if (r < len) {
+            *kq_at(r, dc) = bkr[i];
+            *v_at(r, dc) = bvr[i];
+        }
+    }
+    for (int r = 8 * NB + dj; r < len; r += 8) {                  // longer buffers (drafts below 16)
+        *kq_at(r, dc) = __ldg(reinterpret_cast<const uint4 *>(bk + static_cast<size_t>(r) * 128) + dc);
+        *v_at(r, dc) = __ldg(reinterpret_cast<const uint4 *>(bv + static_cast<size_t>(r) * 128) + dc);
     }
 #pragma unroll
-    for (int i = 0; i < NVV; ++i) {
-        const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
-        *reinterpret_cast<uint4 *>(sV + (c >> 3) * P::SUBV + sw128(r, c & 7)) = vload[i];
-        if (r >= len && r < C) reinterpret_cast<uint4 *>(wv + static_cast<size_t>(r - len) * 128)[c] = vload[i];
+    for (int i = 0; i < 2; ++i) {
+        const int j = dj + 8 * i;
+        if (j < T) {
+            *kq_at(len + j, dc) = draft[i];
+            *kq_at(C + j, dc) = draft[2 + i];
+            *v_at(len + j, dc) = draft[4 + i];
+            reinterpret_cast<uint4 *>(wk + static_cast<size_t>(j) * 128)[dc] = draft[i];
+            reinterpret_cast<uint4 *>(wv + static_cast<size_t>(j) * 128)[dc] = draft[4 + i];
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < P::NPA / 8; ++i) {
+        const int r = dj + 8 * i;
+        if (r >= C + T) *kq_at(r, dc) = make_uint4(0u, 0u, 0u, 0u);
+        if (r >= C && r < CMAX) *v_at(r, dc) = make_uint4(0u, 0u, 0u, 0u);
     }
     if (warp == 0) {                                              // compensated scan of g
         float hi[2], lo[2];

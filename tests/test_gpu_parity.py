@@ -338,3 +338,26 @@ def test_cap63_fused(name):
     pr = Pair(_cap63(name))
     for s in range(14):
         pr.fused_step(s)
+
+
+# ----------------------- short drafts over long buffers (more than 32 buffered rows)
+def _short_draft(name):
+    import dataclasses
+    # cap = 40 - 1 + 8 = 47; accepted counts drawn uniformly in [0, 8]
+    return dataclasses.replace(WL[name], name=name + "_t8", T=8, threshold=40, accept_law="uniform")
+
+
+@pytest.mark.parametrize("name", ["b8", "edge"])
+def test_short_draft_long_buffer_three_call(name):
+    """T = 8 with buffers of up to 39 tokens: rows past the 32 a thread keeps in
+    registers are loaded on a second pass."""
+    pr = Pair(_short_draft(name))
+    for s in range(14):
+        pr.step(s)
+
+
+@pytest.mark.parametrize("name", ["b8", "edge"])
+def test_short_draft_long_buffer_fused(name):
+    pr = Pair(_short_draft(name))
+    for s in range(14):
+        pr.fused_step(s)
