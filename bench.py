@@ -188,6 +188,27 @@ def _accept_pattern(wl, layer, j):
 
 
 # ------------------------------------------------------------------- GPU run
+def layer_seed(l, rank):
+    """Seed of layer l's synthetic checkpoint, buffer and drafts on `rank`: every rank
+    holds its own batch shard (different sequences, the same shapes)."""
+    return l + 100 * rank
+
+
+def max_over_ranks(x, world, device):
+    """The largest of the ranks' values of x (the slowest rank's time); x itself on one rank."""
+    if world == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def per_layer_step_us(ms, steps, layers, world):
+    """Whole-job time per layer-step: `steps` steps of `layers` layers on each of `world`
+    replicas took `ms` (the slowest rank's) milliseconds."""
+    return ms * 1000.0 / (steps * layers * world)
+
+
 def run_ours(args, rank, world, mode="fused"):
     import speculative_decode_recurrent_gb300 as lib
 
@@ -203,12 +224,12 @@ def run_ours(args, rank, world, mode="fused"):
     layers, pools, acc_dev, acc_host = [], [], [], []
     lens0 = []
     for l in range(L):
-        init = synth.initial_layer(wl, l + 100 * rank)
+        init = synth.initial_layer(wl, layer_seed(l, rank))
         layers.append(ReplayLayer(d, init, dev))
         lens0.append(init["buf_len"][init["state_idx"].long()].numpy().astype(np.int64))
-        pools.append([{n: t.to(dev) for n, t in synth.draft_block(wl, l + 100 * rank, s).items()}
+        pools.append([{n: t.to(dev) for n, t in synth.draft_block(wl, layer_seed(l, rank), s).items()}
                       for s in range(DRAFT_POOL)])
-        pats = np.stack([_accept_pattern(wl, l + 100 * rank, j) for j in range(ACCEPT_PERIOD)])
+        pats = np.stack([_accept_pattern(wl, layer_seed(l, rank), j) for j in range(ACCEPT_PERIOD)])
         acc_host.append(pats)
         acc_dev.append(torch.from_numpy(pats).to(dev))
     outs = [torch.empty(wl.B, wl.T, wl.H, wl.dv, device=dev) for _ in range(L)]
@@ -316,11 +337,7 @@ def run_ours(args, rank, world, mode="fused"):
         account(s % ACCEPT_PERIOD)
     torch.cuda.synchronize()
     clocks = clocks_summary(sampler) if rank == 0 else None
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     # the device lengths must follow the host bookkeeping exactly
     for l in range(L):
         got = layers[l].t["buf_len"][layers[l].t["state_idx"].long()].cpu().numpy()
@@ -391,7 +408,7 @@ def run_ours(args, rank, world, mode="fused"):
     # ---- end to end through the public API with host buffers
     e2e = None
     if args.e2e_steps > 0:
-        pin = [{n: t.cpu().pin_memory() for n, t in synth.draft_block(wl, l + 100 * rank, 0).items()}
+        pin = [{n: t.cpu().pin_memory() for n, t in synth.draft_block(wl, layer_seed(l, rank), 0).items()}
                for l in range(L)]
         out_host = [torch.empty_like(outs[l], device="cpu").pin_memory() for l in range(L)]
         stage = [pools[l][0] for l in range(L)]
@@ -428,12 +445,8 @@ def run_ours(args, rank, world, mode="fused"):
                     out_host[l].copy_(outs[l], non_blocking=True)
             x1.record()
         torch.cuda.synchronize()
-        e2e_ms = x0.elapsed_time(x1)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": round(e2e_ms * 1000.0 / (args.e2e_steps * L * world), 3), "unit": "us/layer",
+        e2e_ms = max_over_ranks(x0.elapsed_time(x1), world, dev)
+        e2e = {"value": round(per_layer_step_us(e2e_ms, args.e2e_steps, L, world), 3), "unit": "us/layer",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": args.e2e_steps}
 
@@ -503,7 +516,7 @@ def main():
             L = rr["L"]
             tb = rr["timed_bytes"]
             total_bytes = tb["verify"] + tb["accept"] + tb["flush"]
-            out = {"us_per_layer": round(rr["ms"] * 1000.0 / (args.steps * L * world), 3),
+            out = {"us_per_layer": round(per_layer_step_us(rr["ms"], args.steps, L, world), 3),
                    "hbm_gbs": round(total_bytes / (rr["ms"] * 1e-3) / 1e9 * world, 1),
                    "algorithmic_bytes_per_step": int(total_bytes / args.steps),
                    "tokens_per_s": round(tb["tokens"] / L / (rr["ms"] * 1e-3) * world, 1)}
