@@ -24,6 +24,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -44,9 +45,9 @@ FALLBACK_HBM_GBS = 6800.0
 # dram read+write bytes per verify launch from the ncu capture summarised in
 # profiles/; valid only for the kernel source whose hash is recorded with it.
 NCU_TRAFFIC = {         # {(step mode, source_sha1): dram read + write bytes per launch}
-    ("overlap", "64b983f1656d69f80b3992b0bab513bc00408e8c"): 43.31e6,      # verify_eq_kernel, launch list of profiles/
-    ("three_call", "64b983f1656d69f80b3992b0bab513bc00408e8c"): 43.30e6,   # verify_eq_kernel, launch list of profiles/
-    ("fused", "64b983f1656d69f80b3992b0bab513bc00408e8c"): 48.01e6,        # fold launch 14.05 MB + verify launch 33.96 MB
+    ("overlap", "9ea9cf214077843edbf01d66ef639cf17c6e85df"): 43.31e6,      # verify_eq_kernel, launch list of profiles/
+    ("three_call", "9ea9cf214077843edbf01d66ef639cf17c6e85df"): 43.30e6,   # verify_eq_kernel, launch list of profiles/
+    ("fused", "9ea9cf214077843edbf01d66ef639cf17c6e85df"): 48.01e6,        # fold launch 14.05 MB + verify launch 33.96 MB
 }
 
 
@@ -151,11 +152,20 @@ def hbm_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text):
+    """The source without comments and blank lines (a comment edit keeps the hash)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def source_sha1():
+    """Hash of the kernel sources' code, the key of the recorded ncu traffic."""
     h = hashlib.sha1()
     for rel in ("speculative_decode_recurrent_gb300/csrc/gdn_replay.cu",
-                "speculative_decode_recurrent_gb300/csrc/gdn_replay_tc.cu"):
-        h.update(open(os.path.join(ROOT, rel), "rb").read())
+                "speculative_decode_recurrent_gb300/csrc/gdn_replay_tc.cu",
+                "speculative_decode_recurrent_gb300/csrc/replay_common.h"):
+        h.update(_code_only(open(os.path.join(ROOT, rel)).read()).encode())
     return h.hexdigest()
 
 

@@ -1578,8 +1578,7 @@ int launch_eq(const gdn_replay_dims *d, const ReplayArgs &a, const CUtensorMap &
 }
 
 // Persistent fold launch: as many CTAs as fit at once (two per SM below 113 KB of
-// shared memory; the register count is bounded for two by the launch bounds), at
-// most one per (sequence, head).
+// shared memory; the 224-register cap allows two), at most one per (sequence, head).
 template <bool DRAFT>
 int launch_fold(const gdn_replay_dims *d, const ReplayArgs &a, const CUtensorMap &m, cudaStream_t s) {
     const bool small = d->cap <= 48;
