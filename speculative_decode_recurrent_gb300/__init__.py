@@ -74,6 +74,23 @@ def gdn_replay_strerror(code: int) -> str:
     return load().gdn_replay_strerror(int(code)).decode()
 
 
+def _sizes(d: Dims) -> dict:
+    """Elements of each argument for dims d (the dense layouts of gdnreplay.h)."""
+    B, H, dk, dv, T, cap, n = d.B, d.H, d.dk, d.dv, d.T, d.cap, d.n_slot
+    return {"state": n * H * dv * dk, "state_idx": B, "buf_k": n * H * cap * dk,
+            "buf_v": n * H * cap * dv, "buf_g": n * H * cap, "buf_beta": n * H * cap,
+            "buf_len": n, "q": B * T * H * dk, "k": B * T * H * dk, "v": B * T * H * dv,
+            "g": B * T * H, "beta": B * T * H, "out": B * T * H * dv, "accepted": B, "status": 1}
+
+
+def _check_sizes(d: Dims, **tensors):
+    """Every tensor must hold at least what the kernels read or write for dims d."""
+    need = _sizes(d)
+    for name, t in tensors.items():
+        if isinstance(t, torch.Tensor) and t.numel() < need[name]:
+            raise ValueError(f"{name}: needs at least {need[name]} elements for {d}, got {t.numel()}")
+
+
 def _ptr(t, dtype=None, name=""):
     if t is None:
         return None
@@ -102,6 +119,9 @@ def gdn_replay_verify(d: Dims, state, state_idx, buf_k, buf_v, buf_g, buf_beta, 
                       q, k, v, g, beta, out, status, stream=None):
     tin = _TORCH_IN.get(d.in_dtype)
     f32, i32 = torch.float32, torch.int32
+    _check_sizes(d, state=state, state_idx=state_idx, buf_k=buf_k, buf_v=buf_v, buf_g=buf_g,
+                 buf_beta=buf_beta, buf_len=buf_len, q=q, k=k, v=v, g=g, beta=beta, out=out,
+                 status=status)
     rc = load().gdn_replay_verify(
         ctypes.byref(d), _ptr(state, f32, "state"), _ptr(state_idx, i32, "state_idx"),
         _ptr(buf_k, tin, "buf_k"), _ptr(buf_v, tin, "buf_v"), _ptr(buf_g, f32, "buf_g"),
@@ -116,6 +136,9 @@ def gdn_replay_verify_fold(d: Dims, state, state_idx, buf_k, buf_v, buf_g, buf_b
                            q, k, v, g, beta, out, status, stream=None):
     tin = _TORCH_IN.get(d.in_dtype)
     f32, i32 = torch.float32, torch.int32
+    _check_sizes(d, state=state, state_idx=state_idx, buf_k=buf_k, buf_v=buf_v, buf_g=buf_g,
+                 buf_beta=buf_beta, buf_len=buf_len, q=q, k=k, v=v, g=g, beta=beta, out=out,
+                 status=status)
     rc = load().gdn_replay_verify_fold(
         ctypes.byref(d), _ptr(state, f32, "state"), _ptr(state_idx, i32, "state_idx"),
         _ptr(buf_k, tin, "buf_k"), _ptr(buf_v, tin, "buf_v"), _ptr(buf_g, f32, "buf_g"),
@@ -128,6 +151,7 @@ def gdn_replay_verify_fold(d: Dims, state, state_idx, buf_k, buf_v, buf_g, buf_b
 
 def gdn_replay_accept_fold(d: Dims, buf_len, state_idx, accepted, status, stream=None):
     i32 = torch.int32
+    _check_sizes(d, buf_len=buf_len, state_idx=state_idx, accepted=accepted, status=status)
     rc = load().gdn_replay_accept_fold(ctypes.byref(d), _ptr(buf_len, i32, "buf_len"),
                                        _ptr(state_idx, i32, "state_idx"),
                                        _ptr(accepted, i32, "accepted"), _ptr(status, i32, "status"),
@@ -137,6 +161,7 @@ def gdn_replay_accept_fold(d: Dims, buf_len, state_idx, accepted, status, stream
 
 def gdn_replay_accept(d: Dims, buf_len, state_idx, accepted, status, stream=None):
     i32 = torch.int32
+    _check_sizes(d, buf_len=buf_len, state_idx=state_idx, accepted=accepted, status=status)
     rc = load().gdn_replay_accept(ctypes.byref(d), _ptr(buf_len, i32, "buf_len"),
                                   _ptr(state_idx, i32, "state_idx"),
                                   _ptr(accepted, i32, "accepted"), _ptr(status, i32, "status"),
@@ -148,6 +173,8 @@ def gdn_replay_flush(d: Dims, state, state_idx, buf_k, buf_v, buf_g, buf_beta, b
                      status, stream=None):
     tin = _TORCH_IN.get(d.in_dtype)
     f32, i32 = torch.float32, torch.int32
+    _check_sizes(d, state=state, state_idx=state_idx, buf_k=buf_k, buf_v=buf_v, buf_g=buf_g,
+                 buf_beta=buf_beta, buf_len=buf_len, status=status)
     rc = load().gdn_replay_flush(
         ctypes.byref(d), _ptr(state, f32, "state"), _ptr(state_idx, i32, "state_idx"),
         _ptr(buf_k, tin, "buf_k"), _ptr(buf_v, tin, "buf_v"), _ptr(buf_g, f32, "buf_g"),

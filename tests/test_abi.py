@@ -108,3 +108,24 @@ def test_empty_batch_is_a_noop():
 def test_strerror():
     for c in (0, -1, -2, -3, -4, -99):
         assert isinstance(lib.gdn_replay_strerror(c), str)
+
+
+def test_binding_rejects_undersized_tensors_before_launch():
+    """The Python binding checks every tensor against the dims (the C ABI takes bare
+    pointers and cannot): one element short is refused before anything is launched."""
+    import torch
+    d = good_dims()
+    sizes = lib._sizes(d)
+    f32, bf16, i32 = torch.float32, torch.bfloat16, torch.int32
+    kinds = {"state": f32, "state_idx": i32, "buf_k": bf16, "buf_v": bf16, "buf_g": f32,
+             "buf_beta": f32, "buf_len": i32, "q": bf16, "k": bf16, "v": bf16, "g": f32,
+             "beta": f32, "out": f32, "status": i32}
+    order = ("state", "state_idx", "buf_k", "buf_v", "buf_g", "buf_beta", "buf_len", "q", "k", "v",
+             "g", "beta", "out", "status")
+    for short in order:
+        args = [torch.zeros(sizes[n] - (1 if n == short else 0), dtype=kinds[n]) for n in order]
+        with pytest.raises(ValueError, match=short):
+            lib.gdn_replay_verify(d, *args)
+    with pytest.raises(ValueError, match="accepted"):
+        lib.gdn_replay_accept(d, torch.zeros(sizes["buf_len"], dtype=i32), None,
+                              torch.zeros(sizes["accepted"] - 1, dtype=i32), torch.zeros(1, dtype=i32))
