@@ -227,6 +227,7 @@ def run_ours(args, rank, world, mode="fused"):
     torch.cuda.set_device(dev)
     lib.load()
     from speculative_decode_recurrent_gb300 import Dims, ReplayLayer
+    from speculative_decode_recurrent_gb300.schedule import StepSchedule
     n_slot = wl.n_slot
     d = Dims(B=wl.B, H=wl.H, dk=wl.dk, dv=wl.dv, T=wl.T, cap=wl.cap, threshold=wl.threshold,
              n_slot=n_slot, in_dtype=lib.DTYPE_BF16, scale=wl.scale)
@@ -247,56 +248,20 @@ def run_ours(args, rank, world, mode="fused"):
 
     fused = mode == "fused"
     overlap = mode == "overlap"        # three-call step, each layer's flush on a side stream
-    sides = [torch.cuda.Stream(device=dev) for _ in range(2)]   # layers alternate between them
-    fork = [torch.cuda.Event() for _ in range(L)]
+    sched = StepSchedule(layers, n_side=2, device=dev)
 
     def enqueue_overlap(j, blocks=None, accs=None, marks=None):
-        # the verify of every layer in order on the main stream; the accept and flush
-        # of layer l (needed only by layer l's next verify, one step later) run on one
-        # of two side streams beside the verifies of layers l+1, ...; the step ends
-        # with a join
-        main = torch.cuda.current_stream()
-        if marks is not None:
-            marks[0].record()
-        for l in range(L):
-            blk = pools[l][j % DRAFT_POOL] if blocks is None else blocks[l]
-            acc = acc_dev[l][j] if accs is None else accs[l]
-            layers[l].verify(blk["q"], blk["k"], blk["v"], blk["g"], blk["beta"], outs[l])
-            side = sides[l % len(sides)]
-            fork[l].record(main)
-            side.wait_event(fork[l])
-            with torch.cuda.stream(side):
-                layers[l].accept(acc)
-                layers[l].flush(force=False)
-        if marks is not None:                  # the main stream holds only the verifies
-            marks[1].record()
-        for side in sides:
-            main.wait_stream(side)
+        blocks = [pools[l][j % DRAFT_POOL] for l in range(L)] if blocks is None else blocks
+        accs = [acc_dev[l][j] for l in range(L)] if accs is None else accs
+        sched.enqueue_overlap(blocks, accs, outs, marks=marks)
 
     def enqueue_step(j, events=None):
         if overlap:
             enqueue_overlap(j)
             return
-        for l in range(L):
-            blk = pools[l][j % DRAFT_POOL]
-            if events is not None:
-                events[l][0].record()
-            if fused:
-                layers[l].verify_fold(blk["q"], blk["k"], blk["v"], blk["g"], blk["beta"], outs[l])
-            else:
-                layers[l].verify(blk["q"], blk["k"], blk["v"], blk["g"], blk["beta"], outs[l])
-            if events is not None:
-                events[l][1].record()
-            if fused:
-                layers[l].accept_fold(acc_dev[l][j])
-            else:
-                layers[l].accept(acc_dev[l][j])
-            if events is not None:
-                events[l][2].record()
-            if not fused:
-                layers[l].flush(force=False)
-            if events is not None:
-                events[l][3].record()
+        blocks = [pools[l][j % DRAFT_POOL] for l in range(L)]
+        accs = [acc_dev[l][j] for l in range(L)]
+        sched.enqueue("fused" if fused else "three_call", blocks, accs, outs, events=events)
 
     # one graph per accepted-count pattern (and draft-pool entry)
     graphs = []

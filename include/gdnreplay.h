@@ -75,7 +75,25 @@ typedef struct CUstream_st *cudaStream_t;
 #define GDN_STATUS_NO_ROOM    2   /* verify: buf_len + T > cap; b skipped */
 #define GDN_STATUS_BAD_LEN    4   /* buf_len outside [0, cap] (accept: len + p > cap); b skipped */
 #define GDN_STATUS_BAD_SLOT   8   /* state_idx[b] outside [0, n_slot); b skipped */
-#define GDN_STATUS_TIMEOUT   16   /* a bounded on-chip wait expired; the (b, h) unit was skipped */
+#define GDN_STATUS_TIMEOUT   16   /* a bounded on-chip wait expired; the (b, h) unit was skipped.
+                                     While this bit is set in *status, gdn_replay_flush and
+                                     gdn_replay_accept_fold reset no buffer length (so no
+                                     buffered token is dropped without being folded) */
+#define GDN_STATUS_DRAIN     32   /* after an expired wait, the wait for that unit's own copies and
+                                     tensor-core operations expired too; its tensor memory was
+                                     released anyway (a kernel never hangs), so no result of the
+                                     call may be trusted */
+
+/* Bits of gdn_replay_dims.flags.  Every other bit must be 0 (GDN_ERR_DIMS otherwise). */
+#define GDN_FLAG_TEST_EXPIRE  1   /* test only: every tensor-core kernel takes its wait-expiry exit
+                                     at its first bounded wait, before it has issued any copy or
+                                     tensor-core operation, so the GDN_STATUS_TIMEOUT path runs
+                                     without anything in flight.  Never set in production. */
+
+/* Kernel families (gdn_replay_kernel_family). */
+#define GDN_FAMILY_TCGEN05   1    /* tcgen05 tensor-core kernels: dk = dv = 128, bf16 inputs, T <= 16,
+                                     cap <= 64 */
+#define GDN_FAMILY_PERTOKEN  2    /* per-token CUDA-core kernels: every other valid shape */
 
 typedef struct {
     int32_t B;          /* batch rows (sequences) in this call, >= 0 */
@@ -88,6 +106,7 @@ typedef struct {
     int32_t n_slot;     /* state / buffer slots, >= B */
     int32_t in_dtype;   /* GDN_DTYPE_BF16 or GDN_DTYPE_F32 */
     float   scale;      /* query scale, normally 1/sqrt(dk) */
+    int32_t flags;      /* GDN_FLAG_* bits; 0 in production */
 } gdn_replay_dims;
 
 /*
@@ -168,6 +187,16 @@ int gdn_replay_verify_fold(const gdn_replay_dims *dims,
 int gdn_replay_accept_fold(const gdn_replay_dims *dims, int32_t *buf_len,
                            const int32_t *state_idx, const int32_t *accepted,
                            int32_t *status, cudaStream_t stream);
+
+/*
+ * gdn_replay_kernel_family -- which kernels a verify / flush / verify_fold call with
+ * these dims launches: GDN_FAMILY_TCGEN05 or GDN_FAMILY_PERTOKEN, or a negative
+ * GDN_ERR_* code for dims the calls would reject.  Host only; launches nothing.  A
+ * call whose dims select GDN_FAMILY_TCGEN05 never runs the per-token kernels: if the
+ * tensor-core launch cannot be prepared (for example the driver's tensor-map encoder
+ * cannot be resolved) the call returns GDN_ERR_LAUNCH.
+ */
+int gdn_replay_kernel_family(const gdn_replay_dims *dims);
 
 /* Human-readable text for a GDN_ERR_* code (static storage). */
 const char *gdn_replay_strerror(int code);

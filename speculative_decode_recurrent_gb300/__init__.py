@@ -17,11 +17,17 @@ from . import build as _build
 
 __all__ = ["Dims", "GdnError", "load", "gdn_replay_verify", "gdn_replay_accept",
            "gdn_replay_flush", "gdn_replay_verify_fold", "gdn_replay_accept_fold",
-           "gdn_replay_strerror", "STATUS_BAD_ACCEPT", "STATUS_NO_ROOM", "STATUS_BAD_LEN",
-           "STATUS_BAD_SLOT", "STATUS_TIMEOUT", "DTYPE_BF16", "DTYPE_F32", "ReplayLayer"]
+           "gdn_replay_kernel_family", "gdn_replay_strerror", "STATUS_BAD_ACCEPT",
+           "STATUS_NO_ROOM", "STATUS_BAD_LEN", "STATUS_BAD_SLOT", "STATUS_TIMEOUT",
+           "STATUS_DRAIN", "FLAG_TEST_EXPIRE", "FAMILY_TCGEN05", "FAMILY_PERTOKEN", "DTYPE_BF16",
+           "DTYPE_F32", "ReplayLayer"]
 
 DTYPE_BF16, DTYPE_F32 = 0, 1
 STATUS_BAD_ACCEPT, STATUS_NO_ROOM, STATUS_BAD_LEN, STATUS_BAD_SLOT, STATUS_TIMEOUT = 1, 2, 4, 8, 16
+STATUS_DRAIN = 32
+FLAG_TEST_EXPIRE = 1
+FAMILY_TCGEN05, FAMILY_PERTOKEN = 1, 2
+FAMILY_NAMES = {FAMILY_TCGEN05: "tcgen05", FAMILY_PERTOKEN: "per-token"}
 _TORCH_IN = {DTYPE_BF16: torch.bfloat16, DTYPE_F32: torch.float32}
 
 
@@ -30,7 +36,7 @@ class Dims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("dk", ctypes.c_int32),
                 ("dv", ctypes.c_int32), ("T", ctypes.c_int32), ("cap", ctypes.c_int32),
                 ("threshold", ctypes.c_int32), ("n_slot", ctypes.c_int32),
-                ("in_dtype", ctypes.c_int32), ("scale", ctypes.c_float)]
+                ("in_dtype", ctypes.c_int32), ("scale", ctypes.c_float), ("flags", ctypes.c_int32)]
 
     def __repr__(self):
         return "Dims(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
@@ -63,8 +69,10 @@ def load(rebuild: bool = False) -> ctypes.CDLL:
         lib.gdn_replay_strerror.argtypes = [ctypes.c_int]
         lib.gdn_replay_strerror.restype = ctypes.c_char_p
         lib.gdn_replay_version.argtypes = []
+        lib.gdn_replay_kernel_family.argtypes = [D]
         for f in (lib.gdn_replay_verify, lib.gdn_replay_accept, lib.gdn_replay_flush,
-                  lib.gdn_replay_verify_fold, lib.gdn_replay_accept_fold, lib.gdn_replay_version):
+                  lib.gdn_replay_verify_fold, lib.gdn_replay_accept_fold, lib.gdn_replay_version,
+                  lib.gdn_replay_kernel_family):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -72,6 +80,13 @@ def load(rebuild: bool = False) -> ctypes.CDLL:
 
 def gdn_replay_strerror(code: int) -> str:
     return load().gdn_replay_strerror(int(code)).decode()
+
+
+def gdn_replay_kernel_family(d: Dims) -> int:
+    """FAMILY_TCGEN05 or FAMILY_PERTOKEN: the kernels calls with dims d launch."""
+    rc = load().gdn_replay_kernel_family(ctypes.byref(d))
+    _check("gdn_replay_kernel_family", rc if rc < 0 else 0)
+    return rc
 
 
 def _sizes(d: Dims) -> dict:
@@ -220,3 +235,4 @@ class ReplayLayer:
     def accept_fold(self, accepted, stream=None):
         gdn_replay_accept_fold(self.d, self.t["buf_len"], self.t["state_idx"], accepted,
                                self.status, stream)
+

@@ -278,7 +278,8 @@ __global__ void __launch_bounds__(DV * (DK / 16), 1) verify_fold_pertoken_kernel
 
 // After the flush kernel: one thread per sequence resets the length of every
 // flushed slot (all CTAs of the flush have read it by then) and reports
-// corrupt lengths.
+// corrupt lengths.  When a fold gave up on a bounded wait (GDN_STATUS_TIMEOUT in
+// *status) no length is reset, so no buffered token is dropped unfolded.
 __global__ void flush_lengths_kernel(int32_t *buf_len, const int32_t *state_idx, int B, int n_slot,
                                      int cap, int threshold, int force, int32_t *status)
 {
@@ -286,6 +287,7 @@ __global__ void flush_lengths_kernel(int32_t *buf_len, const int32_t *state_idx,
     pdl_release();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
+    if (*status & GDN_STATUS_TIMEOUT) return;
     const int slot = state_idx ? state_idx[b] : b;
     if (slot < 0 || slot >= n_slot) { atomicOr(status, GDN_STATUS_BAD_SLOT); return; }
     const int len = buf_len[slot];
@@ -311,6 +313,7 @@ __global__ void accept_kernel(int32_t *buf_len, const int32_t *state_idx, const 
 
 // After a verify with fold: sequences whose buffer reached the threshold restart
 // at length 0 (their draft sits in slots 0 .. T-1), then the accepted prefix is kept.
+// After a timed-out verify_fold (GDN_STATUS_TIMEOUT) every length is left as it is.
 __global__ void accept_fold_kernel(int32_t *buf_len, const int32_t *state_idx, const int32_t *accepted,
                                    int B, int n_slot, int T, int cap, int threshold, int32_t *status)
 {
@@ -318,6 +321,7 @@ __global__ void accept_fold_kernel(int32_t *buf_len, const int32_t *state_idx, c
     pdl_release();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
+    if (*status & GDN_STATUS_TIMEOUT) return;
     const int slot = state_idx ? state_idx[b] : b;
     if (slot < 0 || slot >= n_slot) { atomicOr(status, GDN_STATUS_BAD_SLOT); return; }
     const int p = accepted[b];
@@ -339,6 +343,7 @@ int check_dims(const gdn_replay_dims *d) {
     if ((d->dk != 64 && d->dk != 128) || (d->dv != 64 && d->dv != 128)) return GDN_ERR_DIMS;
     if (d->T < 1 || d->T > 64 || d->cap < d->T || d->cap > 256) return GDN_ERR_DIMS;
     if (d->threshold < 1 || d->threshold > d->cap) return GDN_ERR_DIMS;
+    if (d->flags & ~GDN_FLAG_TEST_EXPIRE) return GDN_ERR_DIMS;
     if ((long long)d->B * d->H > 0x7fffffffLL) return GDN_ERR_DIMS;
     if (replay_smem_floats(d->dk, d->dv, d->cap, d->T) * sizeof(float) > 227 * 1024) return GDN_ERR_DIMS;
     return GDN_OK;
@@ -396,7 +401,7 @@ int gdn_replay_verify(const gdn_replay_dims *d, const float *state, const int32_
     a.buf_k = buf_k; a.buf_v = buf_v; a.buf_g = buf_g; a.buf_beta = buf_beta; a.buf_len = buf_len;
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = out; a.status = status;
     a.B = d->B; a.H = d->H; a.T = d->T; a.cap = d->cap; a.threshold = d->threshold;
-    a.n_slot = d->n_slot; a.scale = d->scale;
+    a.n_slot = d->n_slot; a.scale = d->scale; a.flags = d->flags;
     const int tc = gdn::tc_verify(d, a, stream);
     if (tc <= 0) return tc;
     return dispatch_replay<kVerify>(d, a, stream);
@@ -430,7 +435,7 @@ int gdn_replay_flush(const gdn_replay_dims *d, float *state, const int32_t *stat
     a.buf_g = const_cast<float *>(buf_g); a.buf_beta = const_cast<float *>(buf_beta);
     a.buf_len = buf_len; a.status = status;
     a.B = d->B; a.H = d->H; a.T = d->T; a.cap = d->cap; a.threshold = d->threshold;
-    a.force = force ? 1 : 0; a.n_slot = d->n_slot; a.scale = d->scale;
+    a.force = force ? 1 : 0; a.n_slot = d->n_slot; a.scale = d->scale; a.flags = d->flags;
     int r = gdn::tc_flush(d, a, stream);
     if (r > 0) r = dispatch_replay<kFlush>(d, a, stream);
     if (r) return r;
@@ -460,7 +465,7 @@ int gdn_replay_verify_fold(const gdn_replay_dims *d, float *state, const int32_t
     a.buf_k = buf_k; a.buf_v = buf_v; a.buf_g = buf_g; a.buf_beta = buf_beta; a.buf_len = buf_len;
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = out; a.status = status;
     a.B = d->B; a.H = d->H; a.T = d->T; a.cap = d->cap; a.threshold = d->threshold;
-    a.n_slot = d->n_slot; a.scale = d->scale;
+    a.n_slot = d->n_slot; a.scale = d->scale; a.flags = d->flags;
     const int tc = gdn::tc_verify_fold(d, a, stream);
     if (tc <= 0) return tc;
     return dispatch_replay<kVerifyFold>(d, a, stream);
@@ -478,6 +483,12 @@ int gdn_replay_accept_fold(const gdn_replay_dims *d, int32_t *buf_len, const int
                ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
+int gdn_replay_kernel_family(const gdn_replay_dims *d) {
+    const int rc = check_dims(d);
+    if (rc) return rc;
+    return gdn::tc_shape(d) ? GDN_FAMILY_TCGEN05 : GDN_FAMILY_PERTOKEN;
+}
+
 const char *gdn_replay_strerror(int code) {
     switch (code) {
         case GDN_OK: return "ok";
@@ -489,6 +500,6 @@ const char *gdn_replay_strerror(int code) {
     }
 }
 
-int gdn_replay_version(void) { return 100; }
+int gdn_replay_version(void) { return 200; }
 
 }  // extern "C"

@@ -249,9 +249,21 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = a.T, H = a.H, cap = a.cap;
 
+    // fold_class 1: the units that do not fold, in a launch that runs beside the fold
+    // launch preceding it and must not wait for it (every CTA of that launch has
+    // waited for the earlier kernels before letting this one start); CTA (0, 0) waits
+    // for it at the end instead, so the next kernel observes both launches complete.
+    // It reports the length errors of every sequence (the fold launch skips them).
+    const bool split = a.fold_class == 1;
+    const bool waiter = split && blockIdx.x == 0 && blockIdx.y == 0;
+    // GDN_FLAG_TEST_EXPIRE: take the wait-expiry exit at the first bounded wait, with
+    // nothing issued before it
+    const bool expire = (a.flags & GDN_FLAG_TEST_EXPIRE) != 0;
+
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (saddr(smem_raw) & 1023u) {           // the swizzled tiles need a 1024-byte aligned base
         if (tid == 0) atomicOr(a.status, kStatusTimeout);
+        if (waiter) pdl_wait();
         return;
     }
     uint8_t *sV = smem_raw;
@@ -282,13 +294,6 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // fold_class 1: the units that do not fold, in a launch that runs beside the fold
-    // launch preceding it and must not wait for it (every CTA of that launch has
-    // waited for the earlier kernels before letting this one start); CTA (0, 0) waits
-    // for it at the end instead, so the next kernel observes both launches complete.
-    // It reports the length errors of every sequence (the fold launch skips them).
-    const bool split = a.fold_class == 1;
-    const bool waiter = split && blockIdx.x == 0 && blockIdx.y == 0;
     if (!split) pdl_wait();
 
     // ---- the draft rows first: their addresses do not depend on the buffer length,
@@ -458,7 +463,7 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     fence_proxy_async();
     __syncthreads();
     const uint32_t kq0 = saddr(sKQ), v0 = saddr(sV), w0 = saddr(sW), qe0 = saddr(sQe), s00 = saddr(smem_raw);
-    if (tid == 0) {                                               // [K;Q] K^T: coefficients
+    if (tid == 0 && !expire) {                                    // [K;Q] K^T: coefficients
         tc_fence_after();
 #pragma unroll
         for (int q = 0; q < 4; ++q) prefetch_tile_l2(&tm_state, q * 32, ytile);
@@ -487,10 +492,10 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
             sKQ + (tid >> 6) * P::SUBK + sw128(r, (tid & 63) >> 3) + (tid & 7) * 2);
         qcol[t2] = t2 < T ? __bfloat162float(x) : 0.f;
     }
-    bool ok = mbar_wait(&bar[2], 0);
+    bool ok = !expire && mbar_wait(&bar[2], 0);
     if (__syncthreads_or(!ok)) {
         if (tid == 0) {
-            mbar_wait(&bar[2], 0);
+            if (!expire && !mbar_wait(&bar[2], 0)) atomicOr(a.status, GDN_STATUS_DRAIN);
             atomicOr(a.status, kStatusTimeout);
         }
         finish();
@@ -613,7 +618,7 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     ok = mbar_wait(&bar[3], 0);
     if (__syncthreads_or(!ok)) {
         if (tid == 0) {
-            mbar_wait(&bar[3], 0);
+            if (!mbar_wait(&bar[3], 0)) atomicOr(a.status, GDN_STATUS_DRAIN);
             atomicOr(a.status, kStatusTimeout);
         }
         finish();
@@ -672,8 +677,10 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
             }
         }
         if (!good) {                                              // wait (bounded) for what is in flight
-            for (int q = 0; q < mmas; ++q) mbar_wait(&bar[4 + q], 0);
-            for (int i = 0; i < 2; ++i) mbar_wait(&bar[i], (loads[i] - 1) & 1);
+            bool drained = true;
+            for (int q = 0; q < mmas; ++q) drained &= mbar_wait(&bar[4 + q], 0);
+            for (int i = 0; i < 2; ++i) drained &= mbar_wait(&bar[i], (loads[i] - 1) & 1);
+            if (!drained) atomicOr(a.status, GDN_STATUS_DRAIN);
             *flag = 1;
         }
     }
@@ -682,7 +689,7 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     if (ok) ok = mbar_wait(&bar[7], 0);
     if (__syncthreads_or(!ok)) {
         if (tid == 0) {
-            if (*flag == 0) mbar_wait(&bar[7], 0);
+            if (*flag == 0 && !mbar_wait(&bar[7], 0)) atomicOr(a.status, GDN_STATUS_DRAIN);
             atomicOr(a.status, kStatusTimeout);
         }
         finish();
@@ -774,6 +781,8 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
     using P = FoldPlan<CMAX>;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H, cap = a.cap;
+
+    const bool expire = (a.flags & GDN_FLAG_TEST_EXPIRE) != 0;   // see the verify kernel
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (saddr(smem_raw) & 1023u) {
@@ -988,7 +997,7 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
             // and, from an operand starting 64 rows before the key tile, lanes 64..127
             // hold rows 0..63 for columns [ca, Lp); all four warps then build A^T
             const int ca = Lp == 16 ? 16 : ((Lp / 2 + 15) & ~15);
-            if (tid == 0) {                                       // K K^T
+            if (tid == 0 && !expire) {                            // K K^T
                 tc_fence_after();
                 const uint32_t idA = idesc_mn(1, 128, ca), idB = idesc_mn(1, 128, Lp - ca);
                 const uint64_t dKup = desc_sw128(k0 - 8192);
@@ -1006,18 +1015,20 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                 }
                 mma_commit(&bar[0]);
             }
-            if (tid == kPipe) {
+            if (tid == kPipe && !expire) {
                 pk_load(0);
                 pk_load(1);
             }
-            bool ok = mbar_wait(&bar[0], ph);
+            bool ok = !expire && mbar_wait(&bar[0], ph);
             auto drain = [&]() {                                  // after a failed wait: what each issuer started
-                if (tid == 0) mbar_wait(&bar[0], ph);
+                bool drained = true;
+                if (tid == 0 && !expire) drained &= mbar_wait(&bar[0], ph);
                 if (tid == kPipe) {
-                    for (int q = 0; q < pk_mmas; ++q) mbar_wait(&bar[4 + q], ph);
+                    for (int q = 0; q < pk_mmas; ++q) drained &= mbar_wait(&bar[4 + q], ph);
                     for (int i = 0; i < 2; ++i)
-                        if (loads[i]) mbar_wait(&bar[2 + i], (loads[i] - 1) & 1);
+                        if (loads[i]) drained &= mbar_wait(&bar[2 + i], (loads[i] - 1) & 1);
                 }
+                if (!drained) atomicOr(a.status, GDN_STATUS_DRAIN);
                 if (tid == 0) atomicOr(a.status, kStatusTimeout);
             };
             if (__syncthreads_or(!ok)) {
@@ -1207,7 +1218,10 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
             }
             ok = mbar_wait(&bar[1], ph);
             if (__syncthreads_or(!ok)) {
-                if (tid == 0) { mbar_wait(&bar[1], ph); atomicOr(a.status, kStatusTimeout); }
+                if (tid == 0) {
+                    if (!mbar_wait(&bar[1], ph)) atomicOr(a.status, GDN_STATUS_DRAIN);
+                    atomicOr(a.status, kStatusTimeout);
+                }
                 alive = false;
                 break;
             }
@@ -1348,8 +1362,8 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                 ok = mbar_wait(&bar[9], ph);
                 if (__syncthreads_or(!ok)) {
                     if (tid == 0) {
-                        mbar_wait(&bar[8], ph);
-                        mbar_wait(&bar[9], ph);
+                        const bool d8 = mbar_wait(&bar[8], ph), d9 = mbar_wait(&bar[9], ph);
+                        if (!(d8 && d9)) atomicOr(a.status, GDN_STATUS_DRAIN);
                         atomicOr(a.status, kStatusTimeout);
                     }
                     alive = false;
@@ -1424,8 +1438,9 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
             ok = mbar_wait(&bar[8], ph);
             if (__syncthreads_or(!ok)) {
                 if (tid == 0) {
-                    mbar_wait(&bar[8], ph);
-                    if (DRAFT) mbar_wait(&bar[10], ph);
+                    bool drained = mbar_wait(&bar[8], ph);
+                    if (DRAFT) drained &= mbar_wait(&bar[10], ph);
+                    if (!drained) atomicOr(a.status, GDN_STATUS_DRAIN);
                     atomicOr(a.status, kStatusTimeout);
                 }
                 alive = false;
@@ -1473,7 +1488,10 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                 const int T = a.T;
                 ok = mbar_wait(&bar[10], ph);
                 if (__syncthreads_or(!ok)) {
-                    if (tid == 0) { mbar_wait(&bar[10], ph); atomicOr(a.status, kStatusTimeout); }
+                    if (tid == 0) {
+                        if (!mbar_wait(&bar[10], ph)) atomicOr(a.status, GDN_STATUS_DRAIN);
+                        atomicOr(a.status, kStatusTimeout);
+                    }
                     alive = false;
                     break;
                 }
@@ -1507,7 +1525,10 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                 }
                 ok = mbar_wait(&bar[11], ph);
                 if (__syncthreads_or(!ok)) {
-                    if (tid == 0) { mbar_wait(&bar[11], ph); atomicOr(a.status, kStatusTimeout); }
+                    if (tid == 0) {
+                        if (!mbar_wait(&bar[11], ph)) atomicOr(a.status, GDN_STATUS_DRAIN);
+                        atomicOr(a.status, kStatusTimeout);
+                    }
                     alive = false;
                     break;
                 }
@@ -1595,30 +1616,30 @@ int launch_fold(const gdn_replay_dims *d, const ReplayArgs &a, const CUtensorMap
                                                                                  : GDN_ERR_LAUNCH;
 }
 
+}  // namespace
+
 bool tc_shape(const gdn_replay_dims *d) {
     return d->dk == 128 && d->dv == 128 && d->in_dtype == GDN_DTYPE_BF16 && d->T <= 16 && d->cap <= 64;
 }
 
-}  // namespace
-
 int tc_verify(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s) {
     if (!tc_shape(d)) return 1;
     CUtensorMap m;
-    if (!state_map(&m, a.state_in, d->n_slot * d->H * 128)) return 1;
+    if (!state_map(&m, a.state_in, d->n_slot * d->H * 128)) return GDN_ERR_LAUNCH;
     return d->cap <= 48 ? launch_eq<48>(d, a, m, s) : launch_eq<64>(d, a, m, s);
 }
 
 int tc_flush(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s) {
     if (!tc_shape(d)) return 1;
     CUtensorMap m;
-    if (!state_map(&m, a.state_out, d->n_slot * d->H * 128)) return 1;
+    if (!state_map(&m, a.state_out, d->n_slot * d->H * 128)) return GDN_ERR_LAUNCH;
     return launch_fold<false>(d, a, m, s);
 }
 
 int tc_verify_fold(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s) {
     if (!tc_shape(d)) return 1;
     CUtensorMap m;
-    if (!state_map(&m, a.state_out, d->n_slot * d->H * 128)) return 1;
+    if (!state_map(&m, a.state_out, d->n_slot * d->H * 128)) return GDN_ERR_LAUNCH;
     ReplayArgs af = a;                                            // fold the full buffers, verify the draft
     af.force = 0;
     const int rc = launch_fold<true>(d, af, m, s);

@@ -25,6 +25,7 @@ struct ReplayArgs {
     float scale;
     int fold_class;             // 0: all units; 1: only the units that do not fold, launched
                                 // beside the fold launch
+    int flags;                  // gdn_replay_dims.flags (GDN_FLAG_TEST_EXPIRE)
 };
 
 // Programmatic dependent launch: every kernel of the library is launched with
@@ -56,9 +57,10 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 constexpr int32_t kStatusTimeout = GDN_STATUS_TIMEOUT;
 
 // Tensor-core path (gdn_replay_tc.cu): d_k = d_v = 128, bf16 inputs, T <= 16,
-// cap <= 64.  Each returns GDN_OK when it launched, GDN_ERR_LAUNCH on a launch
-// failure, and 1 when the shape is not one it handles (the caller then uses the
-// per-token kernels).
+// cap <= 64 (tc_shape).  Each returns GDN_OK when it launched, GDN_ERR_LAUNCH when
+// the launch (or the tensor map it needs) failed, and 1 only when the shape is not
+// one it handles (the caller then uses the per-token kernels).
+bool tc_shape(const gdn_replay_dims *d);
 int tc_verify(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s);
 int tc_flush(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s);
 // The fused step: the folding sequences (persistent fold kernel, which then verifies

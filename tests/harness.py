@@ -16,6 +16,10 @@ import synth
 
 RTOL_MAX, ATOL = 2e-3, 1e-5
 
+# max|gpu - ref| / max|ref| of every compared tensor, appended by assert_close as
+# (name, ratio); tests that track drift over many steps read it back
+DRIFT = []
+
 
 def gpu_dims(wl: synth.Workload, B=None, n_slot=None):
     import speculative_decode_recurrent_gb300 as lib
@@ -39,7 +43,9 @@ def assert_close(name, got, ref):
     assert got.shape == ref.shape, (name, got.shape, ref.shape)
     assert np.isfinite(got).all(), f"{name}: non-finite values"
     err = float(np.max(np.abs(got - ref))) if got.size else 0.0
-    bound = RTOL_MAX * (float(np.max(np.abs(ref))) if ref.size else 0.0) + ATOL
+    mref = float(np.max(np.abs(ref))) if ref.size else 0.0
+    bound = RTOL_MAX * mref + ATOL
+    DRIFT.append((name, err / mref if mref > 0 else 0.0))
     assert err <= bound, f"{name}: max|d|={err:.3e} > bound {bound:.3e}"
     return err, bound
 

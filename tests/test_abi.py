@@ -37,8 +37,32 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_dims_struct_layout():
-    assert ctypes.sizeof(lib.Dims) == 40
+    assert ctypes.sizeof(lib.Dims) == 44
     assert lib.Dims.scale.offset == 36
+    assert lib.Dims.flags.offset == 40
+
+
+def test_kernel_family_query():
+    """Host-only: which kernels the dims select, and loud rejection of bad dims."""
+    so = lib.load()
+    tc = good_dims(T=16, cap=47, threshold=32)
+    assert so.gdn_replay_kernel_family(ctypes.byref(tc)) == lib.FAMILY_TCGEN05
+    for kw in (dict(dk=64, dv=64), dict(in_dtype=lib.DTYPE_F32), dict(T=17, cap=48, threshold=32),
+               dict(cap=65, threshold=32)):
+        d = good_dims(**kw)
+        assert so.gdn_replay_kernel_family(ctypes.byref(d)) == lib.FAMILY_PERTOKEN, kw
+    assert so.gdn_replay_kernel_family(ctypes.byref(good_dims(dk=96))) == -2
+    assert so.gdn_replay_kernel_family(None) == -1
+    assert lib.gdn_replay_kernel_family(tc) == lib.FAMILY_TCGEN05
+
+
+@pytest.mark.parametrize("flags", [2, 1 << 30, -1])
+def test_unknown_flags_rejected(flags):
+    so = lib.load()
+    d = good_dims(flags=flags)
+    assert so.gdn_replay_verify(ctypes.byref(d), *([FAKE] * 14), None) == -2
+    assert so.gdn_replay_flush(ctypes.byref(d), *([FAKE] * 7), 0, FAKE, None) == -2
+    assert so.gdn_replay_kernel_family(ctypes.byref(d)) == -2
 
 
 def good_dims(**kw):
