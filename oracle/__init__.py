@@ -19,10 +19,15 @@ from dataclasses import dataclass
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "gdn_oracle.c")
+_SRCS = [os.path.join(_HERE, f) for f in ("gdn_oracle.c", "gdn_layer_ops_oracle.c")]
 _LIB = os.path.join(_HERE, "_build", "libgdnoracle.so")
 
 BAD_ACCEPT, NO_ROOM, BAD_LEN = 1, 2, 4
+
+
+class _ConvDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("D", ctypes.c_int), ("W", ctypes.c_int), ("T", ctypes.c_int),
+                ("cap", ctypes.c_int), ("n_slot", ctypes.c_int), ("act", ctypes.c_int)]
 
 
 class _Dims(ctypes.Structure):
@@ -33,11 +38,12 @@ class _Dims(ctypes.Structure):
 
 
 def build(force: bool = False) -> str:
-    """Compile gdn_oracle.c into a shared library with gcc (no -march flags)."""
+    """Compile the oracle's C sources into one shared library with gcc (no -march flags)."""
     os.makedirs(os.path.dirname(_LIB), exist_ok=True)
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    if force or not os.path.exists(_LIB) or any(os.path.getmtime(_LIB) < os.path.getmtime(s)
+                                                 for s in _SRCS):
         tmp = _LIB + f".{os.getpid()}.tmp"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC,
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, *_SRCS,
                                "-lm", "-lpthread"])
         os.replace(tmp, _LIB)
     return _LIB
@@ -58,6 +64,17 @@ def _load():
         lib.orc_accept.argtypes = [ctypes.POINTER(_Dims), P, P, P, P]
         lib.orc_flush.argtypes = [ctypes.POINTER(_Dims)] + [P] * 7 + [ctypes.c_int, P]
         for f in (lib.orc_recur, lib.orc_verify, lib.orc_accept, lib.orc_flush):
+            f.restype = ctypes.c_int
+        CD = ctypes.POINTER(_ConvDims)
+        lib.orc_conv_verify.argtypes = [CD] + [P] * 8
+        lib.orc_conv_accept.argtypes = [CD] + [P] * 4
+        lib.orc_e4m3_decode.argtypes = [ctypes.c_int]
+        lib.orc_e4m3_decode.restype = ctypes.c_double
+        lib.orc_e4m3_encode.argtypes = [ctypes.c_double]
+        lib.orc_e4m3_encode.restype = ctypes.c_int
+        lib.orc_gated_rmsnorm_fp8.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, ctypes.c_double,
+                                              ctypes.c_double, P, P]
+        for f in (lib.orc_conv_verify, lib.orc_conv_accept, lib.orc_gated_rmsnorm_fp8):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -188,3 +205,86 @@ class Layer:
     def flush(self, force: bool = False):
         flush(self.d, self.state, self.state_idx, self.buf_k, self.buf_v, self.buf_g,
               self.buf_beta, self.buf_len, force, self.status)
+
+
+# ------------------------------------------------- causal convolution with rollback
+@dataclass
+class ConvDims:
+    B: int
+    D: int
+    W: int
+    T: int
+    cap: int
+    n_slot: int
+    act: int = 1          # 0 identity, 1 SiLU
+
+    def c(self) -> _ConvDims:
+        return _ConvDims(self.B, self.D, self.W, self.T, self.cap, self.n_slot, self.act)
+
+
+def conv_verify(d: ConvDims, ring, pos, state_idx, x, w, bias, y, status):
+    """Draft outputs of the causal convolution from the committed window (the W-1
+    ring positions before pos) and the draft x; stages x at pos .. pos+T-1 (mod cap)."""
+    args = [_f64(ring, (d.n_slot, d.cap, d.D)), _i32(pos, (d.n_slot,)),
+            None if state_idx is None else _i32(state_idx, (d.B,)),
+            _f64(x, (d.B, d.T, d.D)), _f64(w, (d.D, d.W)),
+            None if bias is None else _f64(bias, (d.D,)), _f64(y, (d.B, d.T, d.D)),
+            _i32(status, (1,))]
+    return _load().orc_conv_verify(ctypes.byref(d.c()), *[_p(a) for a in args])
+
+
+def conv_accept(d: ConvDims, pos, state_idx, accepted, status):
+    """pos += p (mod cap) for 0 <= p <= T: the accepted prefix joins the window."""
+    args = [_i32(pos, (d.n_slot,)), None if state_idx is None else _i32(state_idx, (d.B,)),
+            _i32(accepted, (d.B,)), _i32(status, (1,))]
+    return _load().orc_conv_accept(ctypes.byref(d.c()), *[_p(a) for a in args])
+
+
+class ConvLayer:
+    """One layer's convolution ring and write positions held by the oracle (fp64)."""
+
+    def __init__(self, d: ConvDims, init: dict):
+        self.d = d
+        f = lambda t: np.ascontiguousarray(t.double().numpy())  # noqa: E731  exact widening
+        self.ring = f(init["ring"])
+        self.pos = np.ascontiguousarray(init["pos"].numpy().astype(np.int32))
+        self.state_idx = np.ascontiguousarray(init["state_idx"].numpy().astype(np.int32))
+        self.w = f(init["weight"])
+        self.bias = None if init.get("bias") is None else f(init["bias"])
+        self.status = np.zeros(1, np.int32)
+
+    def verify(self, x) -> np.ndarray:
+        d = self.d
+        y = np.zeros((d.B, d.T, d.D))
+        conv_verify(d, self.ring, self.pos, self.state_idx,
+                    np.ascontiguousarray(x.double().numpy()), self.w, self.bias, y, self.status)
+        return y
+
+    def accept(self, accepted):
+        conv_accept(self.d, self.pos, self.state_idx,
+                    np.ascontiguousarray(np.asarray(accepted, dtype=np.int32)), self.status)
+
+
+# ------------------------------------------------------ gated RMSNorm + E4M3 codes
+def e4m3_decode(code: int) -> float:
+    """Value of an E4M3 code (bias 7, subnormals, NaN at exponent 15 / mantissa 7)."""
+    return _load().orc_e4m3_decode(int(code))
+
+
+def e4m3_encode(x: float) -> int:
+    """E4M3 code of x: round to nearest, ties to even, saturate at +-448."""
+    return _load().orc_e4m3_encode(float(x))
+
+
+def gated_rmsnorm_fp8(o, z, w, eps: float, inv_scale: float):
+    """o, z [rows, d]; w [d].  Returns (codes uint8 [rows, d], y * inv_scale fp64)."""
+    o = np.ascontiguousarray(o, dtype=np.float64)
+    z = np.ascontiguousarray(z, dtype=np.float64)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    rows, d = o.shape
+    assert z.shape == (rows, d) and w.shape == (d,)
+    q = np.zeros((rows, d), np.uint8)
+    yq = np.zeros((rows, d))
+    _load().orc_gated_rmsnorm_fp8(rows, d, _p(o), _p(z), _p(w), float(eps), float(inv_scale),
+                                  _p(q), _p(yq))
+    return q, yq
