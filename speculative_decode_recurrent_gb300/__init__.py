@@ -20,7 +20,8 @@ __all__ = ["Dims", "GdnError", "load", "gdn_replay_verify", "gdn_replay_accept",
            "gdn_replay_kernel_family", "gdn_replay_strerror", "STATUS_BAD_ACCEPT",
            "STATUS_NO_ROOM", "STATUS_BAD_LEN", "STATUS_BAD_SLOT", "STATUS_TIMEOUT",
            "STATUS_DRAIN", "FLAG_TEST_EXPIRE", "FAMILY_TCGEN05", "FAMILY_PERTOKEN", "DTYPE_BF16",
-           "DTYPE_F32", "ReplayLayer"]
+           "DTYPE_F32", "ReplayLayer", "ConvDims", "gdn_conv_verify", "gdn_conv_accept",
+           "gdn_gated_rmsnorm_fp8", "ConvLayer", "CONV_ACT_NONE", "CONV_ACT_SILU"]
 
 DTYPE_BF16, DTYPE_F32 = 0, 1
 STATUS_BAD_ACCEPT, STATUS_NO_ROOM, STATUS_BAD_LEN, STATUS_BAD_SLOT, STATUS_TIMEOUT = 1, 2, 4, 8, 16
@@ -28,6 +29,7 @@ STATUS_DRAIN = 32
 FLAG_TEST_EXPIRE = 1
 FAMILY_TCGEN05, FAMILY_PERTOKEN = 1, 2
 FAMILY_NAMES = {FAMILY_TCGEN05: "tcgen05", FAMILY_PERTOKEN: "per-token"}
+CONV_ACT_NONE, CONV_ACT_SILU = 0, 1
 _TORCH_IN = {DTYPE_BF16: torch.bfloat16, DTYPE_F32: torch.float32}
 
 
@@ -40,6 +42,16 @@ class Dims(ctypes.Structure):
 
     def __repr__(self):
         return "Dims(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
+
+
+class ConvDims(ctypes.Structure):
+    """Mirror of ``gdn_conv_dims`` (include/gdnlayer.h)."""
+    _fields_ = [("B", ctypes.c_int32), ("D", ctypes.c_int32), ("W", ctypes.c_int32),
+                ("T", ctypes.c_int32), ("cap", ctypes.c_int32), ("n_slot", ctypes.c_int32),
+                ("act", ctypes.c_int32), ("in_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32)]
+
+    def __repr__(self):
+        return "ConvDims(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
 
 
 class GdnError(RuntimeError):
@@ -70,6 +82,12 @@ def load(rebuild: bool = False) -> ctypes.CDLL:
         lib.gdn_replay_strerror.restype = ctypes.c_char_p
         lib.gdn_replay_version.argtypes = []
         lib.gdn_replay_kernel_family.argtypes = [D]
+        CD = ctypes.POINTER(ConvDims)
+        lib.gdn_conv_verify.argtypes = [CD] + [P] * 9
+        lib.gdn_conv_accept.argtypes = [CD, P, P, P, P, P]
+        lib.gdn_gated_rmsnorm_fp8.argtypes = [I, I, P, P, I, P, ctypes.c_float, ctypes.c_float, P, P]
+        for f in (lib.gdn_conv_verify, lib.gdn_conv_accept, lib.gdn_gated_rmsnorm_fp8):
+            f.restype = ctypes.c_int
         for f in (lib.gdn_replay_verify, lib.gdn_replay_accept, lib.gdn_replay_flush,
                   lib.gdn_replay_verify_fold, lib.gdn_replay_accept_fold, lib.gdn_replay_version,
                   lib.gdn_replay_kernel_family):
@@ -236,3 +254,73 @@ class ReplayLayer:
         gdn_replay_accept_fold(self.d, self.t["buf_len"], self.t["state_idx"], accepted,
                                self.status, stream)
 
+
+# ------------------------------------------------ causal convolution with rollback
+def _conv_sizes(d: ConvDims) -> dict:
+    return {"ring": d.n_slot * d.cap * d.D, "ring_pos": d.n_slot, "state_idx": d.B,
+            "x": d.B * d.T * d.D, "weight": d.D * d.W, "bias": d.D, "y": d.B * d.T * d.D,
+            "accepted": d.B, "status": 1}
+
+
+def _check_conv_sizes(d: ConvDims, **tensors):
+    need = _conv_sizes(d)
+    for name, t in tensors.items():
+        if isinstance(t, torch.Tensor) and t.numel() < need[name]:
+            raise ValueError(f"{name}: needs at least {need[name]} elements for {d}, got {t.numel()}")
+
+
+def gdn_conv_verify(d: ConvDims, ring, ring_pos, state_idx, x, weight, bias, y, status, stream=None):
+    tin, tout = _TORCH_IN.get(d.in_dtype), _TORCH_IN.get(d.out_dtype)
+    f32, i32 = torch.float32, torch.int32
+    _check_conv_sizes(d, ring=ring, ring_pos=ring_pos, state_idx=state_idx, x=x, weight=weight,
+                      bias=bias, y=y, status=status)
+    rc = load().gdn_conv_verify(
+        ctypes.byref(d), _ptr(ring, tin, "ring"), _ptr(ring_pos, i32, "ring_pos"),
+        _ptr(state_idx, i32, "state_idx"), _ptr(x, tin, "x"), _ptr(weight, f32, "weight"),
+        _ptr(bias, f32, "bias"), _ptr(y, tout, "y"), _ptr(status, i32, "status"), _stream(stream))
+    _check("gdn_conv_verify", rc)
+
+
+def gdn_conv_accept(d: ConvDims, ring_pos, state_idx, accepted, status, stream=None):
+    i32 = torch.int32
+    _check_conv_sizes(d, ring_pos=ring_pos, state_idx=state_idx, accepted=accepted, status=status)
+    rc = load().gdn_conv_accept(ctypes.byref(d), _ptr(ring_pos, i32, "ring_pos"),
+                                _ptr(state_idx, i32, "state_idx"), _ptr(accepted, i32, "accepted"),
+                                _ptr(status, i32, "status"), _stream(stream))
+    _check("gdn_conv_accept", rc)
+
+
+class ConvLayer:
+    """Device-resident convolution ring, write positions, weight and bias of one
+    layer (``init``: CPU tensors ring, pos, state_idx, weight, bias)."""
+
+    def __init__(self, dims: ConvDims, init: dict, device="cuda"):
+        self.d = dims
+        self.t = {n: init[n].to(device).contiguous() for n in ("ring", "pos", "state_idx", "weight")}
+        self.t["bias"] = None if init.get("bias") is None else init["bias"].to(device).contiguous()
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def verify(self, x, y, stream=None):
+        t = self.t
+        gdn_conv_verify(self.d, t["ring"], t["pos"], t["state_idx"], x, t["weight"], t["bias"], y,
+                        self.status, stream)
+
+    def accept(self, accepted, stream=None):
+        gdn_conv_accept(self.d, self.t["pos"], self.t["state_idx"], accepted, self.status, stream)
+
+
+# ---------------------------------------------------- gated RMSNorm + E4M3 codes
+def gdn_gated_rmsnorm_fp8(o, z, weight, eps: float, inv_scale: float, q, stream=None):
+    """o fp32 [rows, d] (any shape whose last dim is d), z bf16/fp32 like o, weight fp32 [d],
+    q uint8 like o (E4M3 codes)."""
+    d = o.shape[-1]
+    rows = o.numel() // d if d else 0
+    if z.numel() != o.numel() or q.numel() != o.numel() or weight.numel() != d:
+        raise ValueError("o, z and q must have the same number of elements; weight must have d")
+    zt = {torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32}.get(z.dtype)
+    if zt is None:
+        raise TypeError(f"z: expected bfloat16 or float32, got {z.dtype}")
+    rc = load().gdn_gated_rmsnorm_fp8(rows, d, _ptr(o, torch.float32, "o"), _ptr(z, None, "z"), zt,
+                                      _ptr(weight, torch.float32, "weight"), float(eps),
+                                      float(inv_scale), _ptr(q, torch.uint8, "q"), _stream(stream))
+    _check("gdn_gated_rmsnorm_fp8", rc)

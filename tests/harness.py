@@ -121,3 +121,68 @@ class Pair:
         np.testing.assert_array_equal(to_np(t["buf_v"]), self.orc.buf_v, err_msg=tag)
         np.testing.assert_array_equal(to_np(t["buf_g"]), self.orc.buf_g, err_msg=tag)
         np.testing.assert_array_equal(to_np(t["buf_beta"]), self.orc.buf_beta, err_msg=tag)
+
+
+# ---------------------------------------------------------- rounded outputs
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """bf16 rounding (nearest, ties to even) of fp64 values.  x is first rounded to
+    fp32, which moves it by at most 2^-24 relative: only values within that of a bf16
+    midpoint can round differently from a single rounding, and every caller widens its
+    comparison by far more than that."""
+    r32 = np.asarray(x, np.float64).astype(np.float32)
+    bits = r32.view(np.uint32)
+    down = (bits & np.uint32(0xFFFF0000))
+    up = down + np.uint32(0x10000)
+    dv, uv = down.view(np.float32).astype(np.float64), up.view(np.float32).astype(np.float64)
+    mid = (dv + uv) / 2
+    mag = np.abs(r32.astype(np.float64))
+    pick_up = (mag > np.abs(mid)) | ((mag == np.abs(mid)) & ((down >> np.uint32(16)) & np.uint32(1)).astype(bool))
+    return np.where(pick_up, uv, dv)
+
+
+def assert_bf16_rounding(name, got_bf16: torch.Tensor, ref: np.ndarray, band: np.ndarray):
+    """got is the bf16 rounding of a value within `band` (absolute, per element) of the
+    fp64 reference, so it must lie between the roundings of ref - band and ref + band
+    (a single value wherever the band does not reach a rounding midpoint).  Returns the
+    count of elements where more than one value is possible."""
+    got = got_bf16.float().cpu().double().numpy().reshape(ref.shape)
+    lo, hi = round_bf16(ref - band), round_bf16(ref + band)
+    ok = (got >= lo) & (got <= hi)
+    bad = np.flatnonzero(~ok)
+    assert bad.size == 0, (f"{name}: {bad.size} elements differ, first at {bad[0]}: got {got.flat[bad[0]]}, "
+                           f"ref {ref.flat[bad[0]]}, allowed [{lo.flat[bad[0]]}, {hi.flat[bad[0]]}]")
+    return int((lo != hi).sum())
+
+
+def _e4m3_round(v: np.ndarray, table: np.ndarray) -> np.ndarray:
+    """E4M3 code of fp64 values (nearest, ties to the even code, saturated at +-448)
+    by search in the table of the 127 non-negative finite values."""
+    pos = table[:0x7F]                                  # codes 0x00 .. 0x7E, increasing
+    mag = np.minimum(np.abs(v), 448.0)
+    i = np.clip(np.searchsorted(pos, mag), 1, 0x7E)     # pos[i-1] < mag <= pos[i]
+    lo, hi = pos[i - 1], pos[i]
+    mid = (lo + hi) / 2
+    code = np.where(mag > mid, i, np.where(mag < mid, i - 1, np.where(i % 2 == 0, i, i - 1)))
+    code = np.where(mag <= pos[0], 0, code)
+    return code | np.where(np.signbit(v), 0x80, 0)
+
+
+def assert_e4m3_codes(name, got_codes: np.ndarray, ref_codes: np.ndarray, ref_value: np.ndarray,
+                      rel_band: float):
+    """E4M3 codes of values within rel_band (relative) of the fp64 ones: each code must be
+    the oracle's, or, where that band reaches a rounding midpoint, a code between the
+    roundings of the band's ends.  Returns the count of elements with more than one
+    possible code."""
+    table = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    got = got_codes.reshape(-1).astype(np.int64)
+    rc = ref_codes.reshape(-1).astype(np.int64)
+    v = ref_value.reshape(-1)
+    lo = _e4m3_round(v - rel_band * np.abs(v), table)
+    hi = _e4m3_round(v + rel_band * np.abs(v), table)
+    assert np.array_equal(_e4m3_round(v, table), rc), f"{name}: the oracle's codes are not its values' rounding"
+    gv, lv, hv = table[got], table[lo], table[hi]
+    ok = (lo == hi) & (got == rc) | (lo != hi) & (gv >= np.minimum(lv, hv)) & (gv <= np.maximum(lv, hv))
+    bad = np.flatnonzero(~ok)
+    assert bad.size == 0, (f"{name}: {bad.size} codes differ, first at {bad[0]}: got {got[bad[0]]:#x}, "
+                           f"ref {rc[bad[0]]:#x} (value {v[bad[0]]!r})")
+    return int((lo != hi).sum())

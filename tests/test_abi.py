@@ -153,3 +153,49 @@ def test_binding_rejects_undersized_tensors_before_launch():
     with pytest.raises(ValueError, match="accepted"):
         lib.gdn_replay_accept(d, torch.zeros(sizes["buf_len"], dtype=i32), None,
                               torch.zeros(sizes["accepted"] - 1, dtype=i32), torch.zeros(1, dtype=i32))
+
+
+# ------------------------------------------ the layer steps either side of the recurrence
+def conv_dims(**kw):
+    d = dict(B=2, D=64, W=4, T=4, cap=8, n_slot=2, act=lib.CONV_ACT_SILU, in_dtype=lib.DTYPE_BF16,
+             out_dtype=lib.DTYPE_BF16)
+    d.update(kw)
+    return lib.ConvDims(**d)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=60), -2), (dict(D=0), -2), (dict(W=0), -2), (dict(W=5), -2), (dict(T=0), -2),
+    (dict(T=65), -2), (dict(cap=6), -2), (dict(n_slot=1), -2), (dict(act=2), -2),
+    (dict(in_dtype=3), -3), (dict(out_dtype=-1), -3), (dict(B=-1), -2),
+])
+def test_conv_bad_dims_rejected_before_launch(kw, code):
+    so = lib.load()
+    d = conv_dims(**kw)
+    assert so.gdn_conv_verify(ctypes.byref(d), *([FAKE] * 8), None) == code
+    assert so.gdn_conv_accept(ctypes.byref(d), FAKE, None, FAKE, FAKE, None) == code
+
+
+def test_conv_null_and_empty():
+    so = lib.load()
+    d = conv_dims()
+    for i in (0, 1, 3, 4, 6, 7):                 # state_idx (2) and bias (5) may be NULL
+        args = [FAKE] * 8
+        args[i] = None
+        assert so.gdn_conv_verify(ctypes.byref(d), *args, None) == -1, i
+    e = conv_dims(B=0, n_slot=0)
+    assert so.gdn_conv_verify(ctypes.byref(e), *([None] * 8), None) == 0
+    assert so.gdn_conv_accept(ctypes.byref(e), None, None, None, None, None) == 0
+
+
+def test_norm_bad_arguments_rejected_before_launch():
+    so = lib.load()
+    args = [FAKE, FAKE, lib.DTYPE_BF16, FAKE, 1e-6, 1.0, FAKE, None]
+    assert so.gdn_gated_rmsnorm_fp8(4, 96, *args) == -2             # d not 64, 128 or 256
+    assert so.gdn_gated_rmsnorm_fp8(-1, 128, *args) == -2
+    bad_z = list(args); bad_z[2] = 5
+    assert so.gdn_gated_rmsnorm_fp8(4, 128, *bad_z) == -3
+    bad_s = list(args); bad_s[5] = 0.0
+    assert so.gdn_gated_rmsnorm_fp8(4, 128, *bad_s) == -2
+    null_q = list(args); null_q[6] = None
+    assert so.gdn_gated_rmsnorm_fp8(4, 128, *null_q) == -1
+    assert so.gdn_gated_rmsnorm_fp8(0, 128, *([None] * 2), 0, None, 1e-6, 1.0, None, None) == 0
