@@ -164,7 +164,8 @@ def source_sha1():
     h = hashlib.sha1()
     for rel in ("speculative_decode_recurrent_gb300/csrc/gdn_replay.cu",
                 "speculative_decode_recurrent_gb300/csrc/gdn_replay_tc.cu",
-                "speculative_decode_recurrent_gb300/csrc/replay_common.h"):
+                "speculative_decode_recurrent_gb300/csrc/replay_common.h",
+                "speculative_decode_recurrent_gb300/csrc/tc_common.cuh"):
         h.update(_code_only(open(os.path.join(ROOT, rel)).read()).encode())
     return h.hexdigest()
 
