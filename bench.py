@@ -60,6 +60,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the other configurations")
     ap.add_argument("--mode", choices=["both", "fused", "three_call", "overlap"], default="both",
                     help="step forms to time; the headline line needs 'both' or 'fused'")
     return ap.parse_args()
@@ -384,47 +385,67 @@ def run_ours(args, rank, world, mode="fused"):
     # ---- end to end through the public API with host buffers
     e2e = None
     if args.e2e_steps > 0:
+        # end to end through the public API with host buffers: every step uploads each
+        # layer's draft block and accepted counts from pinned host memory and reads its
+        # outputs back.  One captured graph per step: the uploads run on a copy stream,
+        # layer l's verify waits only for layer l's upload, and layer l's outputs go back
+        # on a second copy stream as soon as its verify is done, so the transfers of
+        # one layer overlap the kernels of the others.
+        names = ("q", "k", "v", "g", "beta")
         pin = [{n: t.cpu().pin_memory() for n, t in synth.draft_block(wl, layer_seed(l, rank), 0).items()}
                for l in range(L)]
         out_host = [torch.empty_like(outs[l], device="cpu").pin_memory() for l in range(L)]
-        stage = [pools[l][0] for l in range(L)]
+        stage = [{n: torch.empty_like(pools[l][0][n]) for n in names} for l in range(L)]
         acc_stage = [torch.empty(wl.B, dtype=torch.int32, device=dev) for _ in range(L)]
         acc_pin = [torch.from_numpy(acc_host[l][0].copy()).pin_memory() for l in range(L)]
+        cs_in, cs_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        up = [torch.cuda.Event() for _ in range(L)]
+        done = [torch.cuda.Event() for _ in range(L)]
         ge = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             with torch.cuda.graph(ge, stream=stream):
-                if overlap:
-                    enqueue_overlap(0, blocks=stage, accs=acc_stage)
-                for l in range(L if not overlap else 0):
-                    b = stage[l]
-                    if fused:
-                        layers[l].verify_fold(b["q"], b["k"], b["v"], b["g"], b["beta"], outs[l])
-                        layers[l].accept_fold(acc_stage[l])
-                    else:
-                        layers[l].verify(b["q"], b["k"], b["v"], b["g"], b["beta"], outs[l])
-                        layers[l].accept(acc_stage[l])
-                        layers[l].flush(force=False)
+                main = torch.cuda.current_stream()
+                start = torch.cuda.Event()
+                start.record(main)
+                cs_in.wait_event(start)
+                cs_out.wait_event(start)
+                with torch.cuda.stream(cs_in):
+                    for l in range(L):
+                        for n in names:
+                            stage[l][n].copy_(pin[l][n], non_blocking=True)
+                        acc_stage[l].copy_(acc_pin[l], non_blocking=True)
+                        up[l].record(cs_in)
+
+                def before(l):
+                    main.wait_event(up[l])
+
+                def after(l):
+                    done[l].record(main)
+                    cs_out.wait_event(done[l])
+                    with torch.cuda.stream(cs_out):
+                        out_host[l].copy_(outs[l], non_blocking=True)
+
+                sched.enqueue(mode, stage, acc_stage, outs, before=before, after=after)
+                main.wait_stream(cs_in)
+                main.wait_stream(cs_out)
         h2d = sum(sum(t.numel() * t.element_size() for n, t in pin[l].items() if n != "accepted")
                   + acc_pin[l].numel() * 4 for l in range(L))
         d2h = sum(o.numel() * o.element_size() for o in outs)
+        with torch.cuda.stream(stream):
+            ge.replay()
         torch.cuda.synchronize()
         x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             x0.record()
             for s in range(args.e2e_steps):
-                for l in range(L):
-                    for n in ("q", "k", "v", "g", "beta"):
-                        stage[l][n].copy_(pin[l][n], non_blocking=True)
-                    acc_stage[l].copy_(acc_pin[l], non_blocking=True)
                 ge.replay()
-                for l in range(L):
-                    out_host[l].copy_(outs[l], non_blocking=True)
             x1.record()
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(x0.elapsed_time(x1), world, dev)
         e2e = {"value": round(per_layer_step_us(e2e_ms, args.e2e_steps, L, world), 3), "unit": "us/layer",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "steps": args.e2e_steps}
+               "steps": args.e2e_steps,
+               "copies": "per layer, on two copy streams overlapping the other layers' kernels"}
 
     launches_per_step = (3 if fused else 4) * L    # fused: fold launch + the rest + accept_fold
     del graphs, layers, pools
@@ -433,6 +454,129 @@ def run_ours(args, rank, world, mode="fused"):
     return dict(ms=ms, clocks=clocks, timed_bytes=timed_bytes, kern_ms=kern_ms,
                 verify_bpl=verify_bytes_per_launch, flush_bpl=flush_bytes_per_launch, e2e=e2e, L=L,
                 launches_per_step=launches_per_step, mode=mode)
+
+
+# ------------------------------------------------------------ other configurations
+def _graph_total_ms(enqueue, n):
+    """Device time (ms) of enqueue(i) for i < n, captured back to back in one graph and
+    replayed (after one warm-up replay) between a single event pair."""
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i in range(n):
+                enqueue(i)
+        g.replay()
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        s.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def run_extras(args, peak):
+    """The throughput configurations besides the headline sweep -- B=8 (threshold 32),
+    the edge mix (threshold 64, forced accepts, extreme gates), the large batch (B=128,
+    H=32, T=8) -- and the causal convolution and gated RMSNorm + E4M3 kernels at the
+    decode shape.  Each is timed back to back in one captured graph: "cold" rotates over
+    enough independent layers (or input sets) that each call's data has left L2 by the
+    time it comes round again; "l2_warm" repeats one layer (or one input set)."""
+    import speculative_decode_recurrent_gb300 as lib
+    from speculative_decode_recurrent_gb300 import Dims, ReplayLayer
+    from speculative_decode_recurrent_gb300.schedule import StepSchedule
+    from synth.layer_ops import CONV_WORKLOADS, NORM_WORKLOADS, conv_block, initial_conv_layer, norm_inputs
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    out = {}
+    for name in ("b8", "edge", "large"):
+        wl = synth.WORKLOADS[name]
+        d = Dims(B=wl.B, H=wl.H, dk=wl.dk, dv=wl.dv, T=wl.T, cap=wl.cap, threshold=wl.threshold,
+                 n_slot=wl.n_slot, in_dtype=lib.DTYPE_BF16, scale=wl.scale)
+        per_layer = wl.n_slot * wl.H * (wl.dv * wl.dk * 4 + wl.cap * (wl.dk + wl.dv) * 2)
+        n_cold = max(2, int(np.ceil(2 * 129e6 / per_layer)))
+        res = {}
+        for kind, n_layers, steps in (("cold", n_cold, max(2, 64 // n_cold)), ("warm", 1, 32)):
+            inits = [synth.initial_layer(wl, l) for l in range(n_layers)]
+            layers = [ReplayLayer(d, init, dev) for init in inits]
+            lens = [init["buf_len"][init["state_idx"].long()].numpy().astype(np.int64) for init in inits]
+            blocks = [[{n: t.to(dev) for n, t in synth.draft_block(wl, l, s).items()} for s in range(DRAFT_POOL)]
+                      for l in range(n_layers)]
+            accs = [[synth.workloads.accepted_counts(wl, l, 1000 + j).numpy() for j in range(ACCEPT_PERIOD)]
+                    for l in range(n_layers)]
+            acc_dev = [[torch.from_numpy(a).to(dev) for a in al] for al in accs]
+            o = torch.empty(wl.B, wl.T, wl.H, wl.dv, device=dev)
+            sched = [StepSchedule([layers[l]], n_side=1, device=dev) for l in range(n_layers)]
+
+            def enq(i):
+                s, l = divmod(i, n_layers)
+                j = s % ACCEPT_PERIOD
+                sched[l].enqueue_three_call([blocks[l][j % DRAFT_POOL]], [acc_dev[l][j]], [o])
+            n = steps * n_layers
+            ms = _graph_total_ms(enq, n)
+            tot = 0
+            for rep in range(2):                          # the warm-up replay, then the timed one
+                for i in range(n):
+                    s, l = divmod(i, n_layers)
+                    v, a, f, new, _ = bytes_model(wl, lens[l], accs[l][s % ACCEPT_PERIOD])
+                    lens[l] = new
+                    if rep == 1:
+                        tot += v + a + f
+            for layer in layers:
+                if int(layer.status.item()) != 0:
+                    raise RuntimeError(f"{name}: status {int(layer.status.item())}")
+            res[kind] = (ms / n, tot / n, n_layers)
+            del layers, sched
+        t_cold, bpc, nl = res["cold"]
+        gbs = bpc / (t_cold * 1e-3) / 1e9
+        out[name] = {"us_per_layer_step": round(t_cold * 1000, 3), "us_l2_warm": round(res["warm"][0] * 1000, 3),
+                     "algorithmic_bytes_per_step": int(bpc), "hbm_gbs": round(gbs, 1),
+                     "hbm_frac": round(gbs / peak, 4),
+                     "l2": f"cold: {nl} independent layers rotate (more than twice L2); warm: one layer repeated",
+                     "kernels": lib.FAMILY_NAMES[lib.gdn_replay_kernel_family(d)],
+                     "timing": "three-call steps back to back in one captured graph",
+                     "workload": f"B={wl.B}, H={wl.H}, d={wl.dk}, T={wl.T}, threshold {wl.threshold}"}
+    # causal convolution with ring rollback at the decode shape
+    cw = CONV_WORKLOADS["conv_decode"]
+    cd = lib.ConvDims(B=cw.B, D=cw.D, W=cw.W, T=cw.T, cap=cw.cap, n_slot=cw.n_slot, act=cw.act,
+                      in_dtype=lib.DTYPE_BF16, out_dtype=lib.DTYPE_BF16)
+    n_sets = 12                                           # 12 x (ring + x + y) ~ 340 MB
+    cls = [lib.ConvLayer(cd, initial_conv_layer(cw, l), dev) for l in range(n_sets)]
+    xs = [conv_block(cw, l, 0)["x"].to(dev) for l in range(n_sets)]
+    ys = [torch.empty(cw.B, cw.T, cw.D, dtype=torch.bfloat16, device=dev) for _ in range(n_sets)]
+    conv_bytes = cw.B * cw.D * 2 * (3 * cw.T + cw.W - 1) + cw.D * (cw.W + 1) * 4
+    t_cold = _graph_total_ms(lambda i: cls[i % n_sets].verify(xs[i % n_sets], ys[i % n_sets]), 4 * n_sets) / (4 * n_sets)
+    t_warm = _graph_total_ms(lambda i: cls[0].verify(xs[0], ys[0]), 32) / 32
+    gbs = conv_bytes / (t_cold * 1e-3) / 1e9
+    out["conv_verify"] = {"us": round(t_cold * 1000, 3), "us_l2_warm": round(t_warm * 1000, 3),
+                          "algorithmic_bytes": int(conv_bytes), "hbm_gbs": round(gbs, 1),
+                          "hbm_frac": round(gbs / peak, 4),
+                          "l2": f"cold: {n_sets} input sets rotate (more than twice L2)",
+                          "workload": f"B={cw.B}, D={cw.D} channels, W={cw.W}, T={cw.T}, bf16 in/out"}
+    for c in cls:
+        if int(c.status.item()) != 0:
+            raise RuntimeError(f"conv status {int(c.status.item())}")
+    del cls, xs, ys
+    nw = NORM_WORKLOADS["norm_decode"]
+    n_sets = 40                                           # 40 x 7.3 MB
+    nis = [{k: v.to(dev) for k, v in norm_inputs(nw, seed_offset=l).items()} for l in range(n_sets)]
+    qs = [torch.empty(nis[0]["o"].shape, dtype=torch.uint8, device=dev) for _ in range(n_sets)]
+
+    def norm_call(i):
+        ni = nis[i % n_sets]
+        lib.gdn_gated_rmsnorm_fp8(ni["o"], ni["z"], ni["weight"], nw.eps, nw.inv_scale, qs[i % n_sets])
+    norm_bytes = nw.rows * nw.d * (4 + 2 + 1) + nw.d * 4
+    t_cold = _graph_total_ms(norm_call, 2 * n_sets) / (2 * n_sets)
+    t_warm = _graph_total_ms(lambda i: norm_call(0), 32) / 32
+    gbs = norm_bytes / (t_cold * 1e-3) / 1e9
+    out["gated_rmsnorm_fp8"] = {"us": round(t_cold * 1000, 3), "us_l2_warm": round(t_warm * 1000, 3),
+                                "algorithmic_bytes": int(norm_bytes), "hbm_gbs": round(gbs, 1),
+                                "hbm_frac": round(gbs / peak, 4),
+                                "l2": f"cold: {n_sets} input sets rotate (more than twice L2)",
+                                "workload": f"{nw.rows} rows of d={nw.d} (B=32, T=16, H=16), bf16 gate"}
+    torch.cuda.synchronize()
+    return out
 
 
 def main():
@@ -532,10 +676,17 @@ def main():
                                "into the next verify)",
                       "three_call": "gdn_replay_verify + gdn_replay_accept + gdn_replay_flush per layer, "
                                     "one stream"}
+        extras = None if args.no_extras else run_extras(args, peak)
+        import speculative_decode_recurrent_gb300 as lib
+        hd = lib.Dims(B=wl.B, H=wl.H, dk=wl.dk, dv=wl.dv, T=wl.T, cap=wl.cap, threshold=wl.threshold,
+                      n_slot=wl.n_slot, in_dtype=lib.DTYPE_BF16, scale=wl.scale)
         line = {"metric": metric, "value": s_h["us_per_layer"], "unit": "us/layer", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": round(head["ms"] / args.steps, 4), "higher_is_better": False,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, f32 state/accumulate",
+                "precision": "q, k, v bf16; state, gates, outputs fp32; checkpoint contractions tf32 "
+                             "(one pass), token-side contractions bf16 hi+lo split, fp32 accumulation",
+                "kernels": lib.FAMILY_NAMES[lib.gdn_replay_kernel_family(hd)], "data": "synthetic",
                 "config": {"workload": workload_desc, "step": steps_desc[head["mode"]],
                            "l2": "inputs larger than L2 (24 layers x 33.5 MB state rotate per step)",
                            "parallelism": f"replicas x{world} (batch-sharded, no collective)",
@@ -544,7 +695,8 @@ def main():
                 "hbm_frac": s_h["hbm_frac"],
                 "algorithmic_bytes_per_step": s_h["algorithmic_bytes_per_step"],
                 "roofline": roof_h, "cpu_baseline": cpu, "e2e": head["e2e"],
-                "gpu_launches": head["launches_per_step"] * args.steps, "clocks": head["clocks"]}
+                "gpu_launches": head["launches_per_step"] * args.steps, "clocks": head["clocks"],
+                "other_configs": extras}
         if head is not r:
             line["fused"] = dict(s_f, step=steps_desc["fused"], roofline=roof_f, e2e=r["e2e"],
                                  clocks=r["clocks"], gpu_launches=r["launches_per_step"] * args.steps)

@@ -44,8 +44,8 @@ extern "C" {
  *   ring_pos  int32     [n_slot]        0 <= ring_pos < cap
  *   state_idx int32     [B]             slot of sequence b; NULL = identity
  *   x         in_dtype  [B, T, D]       draft inputs (pre-convolution)
- *   weight    fp32      [D, W]          weight[c][W-1] multiplies the current input
- *   bias      fp32      [D] or NULL
+ *   weight    fp32      [D, W]          weight[c][W-1] multiplies the current input; 16-byte aligned
+ *   bias      fp32      [D] or NULL (16-byte aligned)
  *   y         out_dtype [B, T, D]
  *   accepted  int32     [B]             0..T
  * Arithmetic in fp32; a bf16 y is rounded to nearest even once at the end.

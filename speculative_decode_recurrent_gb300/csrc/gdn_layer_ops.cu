@@ -22,8 +22,8 @@ using gdn::pdl_release;
 using gdn::pdl_wait;
 
 constexpr int kConvThreads = 128;
-constexpr int kTaps = 4;            // widest kernel; narrower ones get leading zero taps
-constexpr int kChunk = 8;           // draft tokens whose loads are in flight together
+constexpr int kTaps = 4;            // widest kernel
+constexpr int kChunk = 8;           // draft positions per thread
 
 struct ConvArgs {
     void *ring;
@@ -36,38 +36,28 @@ struct ConvArgs {
     int B, D, W, T, cap, n_slot, act;
 };
 
-// 16 bytes of inputs <-> floats
-__device__ __forceinline__ void unpack(const uint4 &r, float (&f)[8]) {
-    const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&r);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 v = __bfloat1622float2(p[i]);
-        f[2 * i] = v.x;
-        f[2 * i + 1] = v.y;
+// Four consecutive channels of an input row: 8 bytes of bf16 or 16 bytes of fp32.
+template <typename TIn> struct In4;
+template <> struct In4<__nv_bfloat16> {
+    using Raw = uint2;
+    __device__ static void unpack(const uint2 &r, float (&f)[4]) {
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.y));
+        f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
     }
-}
-__device__ __forceinline__ void unpack(const uint4 &r, float (&f)[4]) {
-    f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
-    f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
-}
-
-template <typename T> struct Vec { static constexpr int N = 16 / sizeof(T); };
-
-template <typename TOut, int V>
-__device__ __forceinline__ void store_out(TOut *dst, const float (&v)[V]);
-template <>
-__device__ __forceinline__ void store_out<__nv_bfloat16, 8>(__nv_bfloat16 *dst, const float (&v)[8]) {
-    uint4 r;
-    uint32_t *w = reinterpret_cast<uint32_t *>(&r);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat162 p = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-        w[i] = *reinterpret_cast<const uint32_t *>(&p);
+};
+template <> struct In4<float> {
+    using Raw = uint4;
+    __device__ static void unpack(const uint4 &r, float (&f)[4]) {
+        f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
+        f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
     }
-    *reinterpret_cast<uint4 *>(dst) = r;
-}
+};
+
+template <typename TOut>
+__device__ __forceinline__ void store_out4(TOut *dst, const float (&v)[4]);
 template <>
-__device__ __forceinline__ void store_out<__nv_bfloat16, 4>(__nv_bfloat16 *dst, const float (&v)[4]) {
+__device__ __forceinline__ void store_out4<__nv_bfloat16>(__nv_bfloat16 *dst, const float (&v)[4]) {
     uint2 r;
     const __nv_bfloat162 p0 = __floats2bfloat162_rn(v[0], v[1]), p1 = __floats2bfloat162_rn(v[2], v[3]);
     r.x = *reinterpret_cast<const uint32_t *>(&p0);
@@ -75,100 +65,89 @@ __device__ __forceinline__ void store_out<__nv_bfloat16, 4>(__nv_bfloat16 *dst, 
     *reinterpret_cast<uint2 *>(dst) = r;
 }
 template <>
-__device__ __forceinline__ void store_out<float, 8>(float *dst, const float (&v)[8]) {
-    reinterpret_cast<float4 *>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
-    reinterpret_cast<float4 *>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
-}
-template <>
-__device__ __forceinline__ void store_out<float, 4>(float *dst, const float (&v)[4]) {
+__device__ __forceinline__ void store_out4<float>(float *dst, const float (&v)[4]) {
     *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
 }
 
-// One thread owns V consecutive channels (one 16-byte input vector) of one
-// sequence for every position: it reads the W-1 window vectors, then the draft
-// vectors in chunks whose loads are all in flight before the first is used, emits
-// the T outputs and stages the raw draft vectors in the ring.  No two threads touch
-// the same bytes, so reading the window before staging needs no barrier.
-template <typename TIn, typename TOut>
+// One thread owns 4 consecutive channels of one sequence for a chunk of kChunk draft
+// positions (a warp covers 128 channels: whole 128-byte lines for bf16 rows): it reads
+// the W-1 inputs before its chunk (from the ring for the first chunk, from the draft
+// otherwise) and the chunk's draft inputs, all requested before the first is used,
+// emits the outputs and stages its raw draft inputs in the ring.  Staged positions
+// pos .. pos+T-1 never meet the window pos-W+1 .. pos-1 (cap >= W - 1 + T), and no two
+// threads write the same bytes, so no barrier is needed.  About 60 registers: the
+// whole grid is resident at once.
+template <typename TIn, typename TOut, int W>
 __global__ void __launch_bounds__(kConvThreads) conv_verify_kernel(const ConvArgs a)
 {
-    constexpr int V = Vec<TIn>::N;
-    const int b = blockIdx.y;
-    const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * V;
+    using Raw = typename In4<TIn>::Raw;
+    const int b = blockIdx.y, t0 = blockIdx.z * kChunk;
+    const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * 4;
     pdl_wait();
     pdl_release();
     if (c0 >= a.D) return;
     const int slot = a.state_idx ? a.state_idx[b] : b;
     if (slot < 0 || slot >= a.n_slot) {
-        if (c0 == 0) atomicOr(a.status, GDN_STATUS_BAD_SLOT);
+        if (c0 == 0 && t0 == 0) atomicOr(a.status, GDN_STATUS_BAD_SLOT);
         return;
     }
     const int pos = a.ring_pos[slot];
     if (pos < 0 || pos >= a.cap) {
-        if (c0 == 0) atomicOr(a.status, GDN_STATUS_BAD_LEN);
+        if (c0 == 0 && t0 == 0) atomicOr(a.status, GDN_STATUS_BAD_LEN);
         return;
     }
-    const int D = a.D, W = a.W, T = a.T, cap = a.cap;
+    const int D = a.D, T = a.T, cap = a.cap;
     TIn *ring = reinterpret_cast<TIn *>(a.ring) + static_cast<size_t>(slot) * cap * D + c0;
     const TIn *x = reinterpret_cast<const TIn *>(a.x) + static_cast<size_t>(b) * T * D + c0;
     TOut *y = reinterpret_cast<TOut *>(a.y) + static_cast<size_t>(b) * T * D + c0;
 
-    // window: h[j] is input x_{j-3}; only the last W-1 exist for this kernel width
-    uint4 hraw[kTaps - 1];
+    // inputs x_{t0-W+1} .. x_{t0-1}, then the chunk
+    Raw hraw[W > 1 ? W - 1 : 1], xr[kChunk];
 #pragma unroll
-    for (int j = 0; j < kTaps - 1; ++j) {
-        hraw[j] = make_uint4(0u, 0u, 0u, 0u);
-        if (j >= kTaps - W) {
-            const int r = (pos - (kTaps - 1) + j + cap) % cap;
-            hraw[j] = *reinterpret_cast<const uint4 *>(ring + static_cast<size_t>(r) * D);
-        }
+    for (int j = 0; j < W - 1; ++j) {
+        const int u = t0 - (W - 1) + j;
+        const TIn *src = u >= 0 ? x + static_cast<size_t>(u) * D : ring + static_cast<size_t>((pos + u + cap) % cap) * D;
+        hraw[j] = __ldg(reinterpret_cast<const Raw *>(src));
     }
-    // taps padded on the left: wt[i][j] multiplies x_{t-3+j}
-    float wt[V][kTaps], bias[V];
 #pragma unroll
-    for (int i = 0; i < V; ++i) {
-        bias[i] = a.bias ? __ldg(a.bias + c0 + i) : 0.f;
-#pragma unroll
-        for (int j = 0; j < kTaps; ++j) {
-            const int jj = j - (kTaps - W);
-            wt[i][j] = jj >= 0 ? __ldg(a.weight + static_cast<size_t>(c0 + i) * W + jj) : 0.f;
-        }
+    for (int u = 0; u < kChunk; ++u) {
+        if (t0 + u < T) xr[u] = __ldg(reinterpret_cast<const Raw *>(x + static_cast<size_t>(t0 + u) * D));
     }
-    float h[kTaps - 1][V];
+    // the 4 channels' taps: 4 W consecutive floats
+    float wt[4 * W], bias[4];
 #pragma unroll
-    for (int j = 0; j < kTaps - 1; ++j) unpack(hraw[j], h[j]);
-
-    for (int t0 = 0; t0 < T; t0 += kChunk) {
-        uint4 xr[kChunk];
+    for (int q = 0; q < W; ++q) {
+        const float4 w4 = __ldg(reinterpret_cast<const float4 *>(a.weight + static_cast<size_t>(c0) * W) + q);
+        wt[4 * q] = w4.x; wt[4 * q + 1] = w4.y; wt[4 * q + 2] = w4.z; wt[4 * q + 3] = w4.w;
+    }
+    if (a.bias) {
+        const float4 b4 = __ldg(reinterpret_cast<const float4 *>(a.bias + c0));
+        bias[0] = b4.x; bias[1] = b4.y; bias[2] = b4.z; bias[3] = b4.w;
+    } else {
+        bias[0] = bias[1] = bias[2] = bias[3] = 0.f;
+    }
+    float h[W][4];                                       // h[W-1] is the current input
 #pragma unroll
-        for (int u = 0; u < kChunk; ++u)
-            xr[u] = t0 + u < T ? __ldg(reinterpret_cast<const uint4 *>(x + static_cast<size_t>(t0 + u) * D))
-                               : make_uint4(0u, 0u, 0u, 0u);
+    for (int j = 0; j < W - 1; ++j) In4<TIn>::unpack(hraw[j], h[j]);
 #pragma unroll
-        for (int u = 0; u < kChunk; ++u) {
-            const int t = t0 + u;
-            if (t >= T) break;
-            float xv[V], o[V];
-            unpack(xr[u], xv);
+    for (int u = 0; u < kChunk; ++u) {
+        const int t = t0 + u;
+        if (t >= T) break;
+        In4<TIn>::unpack(xr[u], h[W - 1]);
+        float o[4];
 #pragma unroll
-            for (int i = 0; i < V; ++i) {
-                float acc = bias[i];
-                acc = fmaf(wt[i][0], h[0][i], acc);
-                acc = fmaf(wt[i][1], h[1][i], acc);
-                acc = fmaf(wt[i][2], h[2][i], acc);
-                acc = fmaf(wt[i][3], xv[i], acc);
-                o[i] = a.act == GDN_CONV_ACT_SILU ? acc / (1.f + expf(-acc)) : acc;
-            }
-            store_out<TOut, V>(y + static_cast<size_t>(t) * D, o);
-            const int r = (pos + t) % cap;
-            *reinterpret_cast<uint4 *>(ring + static_cast<size_t>(r) * D) = xr[u];
+        for (int i = 0; i < 4; ++i) {
+            float acc = bias[i];
 #pragma unroll
-            for (int i = 0; i < V; ++i) {
-                h[0][i] = h[1][i];
-                h[1][i] = h[2][i];
-                h[2][i] = xv[i];
-            }
+            for (int j = 0; j < W; ++j) acc = fmaf(wt[i * W + j], h[j][i], acc);
+            o[i] = a.act == GDN_CONV_ACT_SILU ? __fdividef(acc, 1.f + __expf(-acc)) : acc;   // 0 below -87
         }
+        store_out4<TOut>(y + static_cast<size_t>(t) * D, o);
+        *reinterpret_cast<Raw *>(ring + static_cast<size_t>((pos + t) % cap) * D) = xr[u];
+#pragma unroll
+        for (int j = 0; j + 1 < W; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) h[j][i] = h[j + 1][i];
     }
 }
 
@@ -245,7 +224,7 @@ __global__ void __launch_bounds__(kNormWarps * 32) gated_rmsnorm_fp8_kernel(
         float v[2];
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-            const float g = zv[i + k] / (1.f + expf(-zv[i + k]));
+            const float g = __fdividef(zv[i + k], 1.f + __expf(-zv[i + k]));   // silu; 0 below -87
             v[k] = ov[i + k] * r * wv[i + k] * g * inv_scale;
         }
         const __nv_fp8x2_storage_t p = __nv_cvt_float2_to_fp8x2(make_float2(v[0], v[1]), __NV_SATFINITE, __NV_E4M3);
@@ -280,13 +259,22 @@ int check_conv(const gdn_conv_dims *d) {
     return GDN_OK;
 }
 
+template <typename TIn, typename TOut, int W>
+int launch_conv_w(const gdn_conv_dims *d, const ConvArgs &a, cudaStream_t s) {
+    const int vecs = d->D / 4;
+    const dim3 grid((vecs + kConvThreads - 1) / kConvThreads, d->B, (d->T + kChunk - 1) / kChunk);
+    return launch_pdl(conv_verify_kernel<TIn, TOut, W>, grid, dim3(kConvThreads), 0, s, a) == cudaSuccess
+               ? GDN_OK : GDN_ERR_LAUNCH;
+}
+
 template <typename TIn, typename TOut>
 int launch_conv(const gdn_conv_dims *d, const ConvArgs &a, cudaStream_t s) {
-    constexpr int V = Vec<TIn>::N;
-    const int vecs = d->D / V;
-    const dim3 grid((vecs + kConvThreads - 1) / kConvThreads, d->B);
-    return launch_pdl(conv_verify_kernel<TIn, TOut>, grid, dim3(kConvThreads), 0, s, a) == cudaSuccess
-               ? GDN_OK : GDN_ERR_LAUNCH;
+    switch (d->W) {
+        case 1: return launch_conv_w<TIn, TOut, 1>(d, a, s);
+        case 2: return launch_conv_w<TIn, TOut, 2>(d, a, s);
+        case 3: return launch_conv_w<TIn, TOut, 3>(d, a, s);
+        default: return launch_conv_w<TIn, TOut, 4>(d, a, s);
+    }
 }
 
 template <int D>
@@ -314,8 +302,8 @@ int gdn_conv_verify(const gdn_conv_dims *d, void *ring, const int32_t *ring_pos,
     if (rc) return rc;
     if (d->B == 0) return GDN_OK;
     if (!ring || !ring_pos || !x || !weight || !y || !status) return GDN_ERR_NULL;
-    if (!aligned(ring, 16) || !aligned(x, 16) || !aligned(y, 16) || !aligned(weight, 4) ||
-        (bias && !aligned(bias, 4)))
+    if (!aligned(ring, 16) || !aligned(x, 16) || !aligned(y, 16) || !aligned(weight, 16) ||
+        (bias && !aligned(bias, 16)))
         return GDN_ERR_DIMS;
     ConvArgs a{ring, ring_pos, state_idx, x, weight, bias, y, status,
                d->B, d->D, d->W, d->T, d->cap, d->n_slot, d->act};

@@ -17,6 +17,9 @@ they may run beside the verifies of the later layers.  Three orders of the same 
 
 All three may be captured in a CUDA graph (the side streams fork from and join the
 capturing stream).  They only enqueue library calls; every step runs in the kernels.
+The optional hooks ``before(l)`` / ``after(l)`` run on the host right before layer
+l's verify is enqueued and right after it, on the current stream (e.g. to wait for
+that layer's inputs to arrive, or to start copying its outputs out).
 """
 from __future__ import annotations
 
@@ -31,7 +34,7 @@ class StepSchedule:
         self.sides = [torch.cuda.Stream(device=device) for _ in range(n_side)]
         self.fork = [torch.cuda.Event() for _ in self.layers]
 
-    def enqueue_overlap(self, blocks, accepted, outs, marks=None):
+    def enqueue_overlap(self, blocks, accepted, outs, marks=None, before=None, after=None):
         """blocks[l]: dict of device draft tensors (q, k, v, g, beta); accepted[l]:
         device int32 [B]; outs[l]: device fp32 [B, T, H, dv].  ``marks`` (two timing
         events) bracket the run of verifies on the current stream."""
@@ -40,7 +43,11 @@ class StepSchedule:
             marks[0].record()
         for l, layer in enumerate(self.layers):
             b = blocks[l]
+            if before is not None:
+                before(l)
             layer.verify(b["q"], b["k"], b["v"], b["g"], b["beta"], outs[l])
+            if after is not None:
+                after(l)
             side = self.sides[l % len(self.sides)]
             self.fork[l].record(main)
             side.wait_event(self.fork[l])
@@ -52,13 +59,17 @@ class StepSchedule:
         for side in self.sides:
             main.wait_stream(side)
 
-    def enqueue_three_call(self, blocks, accepted, outs, events=None):
+    def enqueue_three_call(self, blocks, accepted, outs, events=None, before=None, after=None):
         """``events[l]`` (four timing events, optional) bracket layer l's calls."""
         for l, layer in enumerate(self.layers):
             b = blocks[l]
+            if before is not None:
+                before(l)
             if events is not None:
                 events[l][0].record()
             layer.verify(b["q"], b["k"], b["v"], b["g"], b["beta"], outs[l])
+            if after is not None:
+                after(l)
             if events is not None:
                 events[l][1].record()
             layer.accept(accepted[l])
@@ -68,12 +79,16 @@ class StepSchedule:
             if events is not None:
                 events[l][3].record()
 
-    def enqueue_fused(self, blocks, accepted, outs, events=None):
+    def enqueue_fused(self, blocks, accepted, outs, events=None, before=None, after=None):
         for l, layer in enumerate(self.layers):
             b = blocks[l]
+            if before is not None:
+                before(l)
             if events is not None:
                 events[l][0].record()
             layer.verify_fold(b["q"], b["k"], b["v"], b["g"], b["beta"], outs[l])
+            if after is not None:
+                after(l)
             if events is not None:
                 events[l][1].record()
             layer.accept_fold(accepted[l])

@@ -4,8 +4,8 @@ against the CPU oracle on the same seeded inputs.
 
 Tolerances, derived from the arithmetic (fp32 on the GPU, fp64 in the oracle):
 * convolution, fp32 y: each output is bias + W <= 4 fused multiply-adds and a SiLU
-  (expf and one division, a few ulp), so |d| <= 2^-20 S + 1e-7 with
-  S = |bias| + sum_j |w_j x_j| per element;
+  (__expf and __fdividef, relative error about 2^-21 each), so |d| <= 2^-20 S + 1e-7
+  with S = |bias| + sum_j |w_j x_j| per element;
 * convolution, bf16 y: the bf16 rounding of that fp32 value: exact wherever the fp64
   value is farther than that bound from a rounding midpoint, else either neighbour;
 * norm codes: every factor is a product (no cancellation), so the fp32 value is within
