@@ -447,7 +447,9 @@ def run_ours(args, rank, world, mode="fused"):
                "steps": args.e2e_steps,
                "copies": "per layer, on two copy streams overlapping the other layers' kernels"}
 
-    launches_per_step = (3 if fused else 4) * L    # fused: fold launch + the rest + accept_fold
+    # fused: fold launch + verify launch + accept_fold; three-call: verify + accept + fold
+    # + lengths
+    launches_per_step = (3 if fused else 4) * L
     del graphs, layers, pools
     torch.cuda.synchronize()
     torch.cuda.empty_cache()

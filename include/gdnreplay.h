@@ -92,7 +92,7 @@ typedef struct CUstream_st *cudaStream_t;
 
 /* Kernel families (gdn_replay_kernel_family). */
 #define GDN_FAMILY_TCGEN05   1    /* tcgen05 tensor-core kernels: dk = dv = 128, bf16 inputs, T <= 16,
-                                     cap <= 64 */
+                                     cap <= 80 */
 #define GDN_FAMILY_PERTOKEN  2    /* per-token CUDA-core kernels: every other valid shape */
 
 typedef struct {

@@ -59,7 +59,7 @@ constexpr int kFoldRegs = 224;
 // The checkpoint enters a single M = 128, N = 16 contraction; everything else
 // depends on the tokens only.  W comes from the back substitution
 // W[t2][s] = M[t2][s] - sum_{s' > s} W[t2][s'] A[s'][s], one warp per four draft
-// rows and one lane per two token columns; qe and ve are bf16 contractions of the
+// rows and one lane per token column modulo 32; qe and ve are bf16 contractions of the
 // key and value rows (read as MN-major operands, no transpose) with W beta gamma
 // and W beta split into two bf16 terms each (relative error 2^-16).
 // The checkpoint is prefetched into L2 at the start and streamed through two
@@ -71,7 +71,8 @@ constexpr int kFoldRegs = 224;
 //   [OFF_A, +CMAX^2 4)   A, fp32, row-major [CMAX][CMAX]
 //   [OFF_M, +16 CMAX 4)  M, fp32, row-major [16][CMAX]
 //   [OFF_A, +8K)         after the back substitution: W beta gamma and W beta as 2 + 2
-//                        bf16 tiles [16][64]
+//                        bf16 tiles [16][64]; CMAX = 80: token columns 64..79 in 2 + 2
+//                        tiles [16][16] with 32-byte swizzle at [OFF_A + 8K, +2K)
 //   [0, 32K)             after the token contractions: two checkpoint quarter buffers
 //   [OFF_QE, +8K)        then qe as fp32 [16][128] (4 sub-tiles of 16 rows x 128 B)
 //   [OFF_S, ...)         8 mbarriers, TMEM slot, flag, then G (hi, lo), beta, gamma
@@ -81,6 +82,9 @@ constexpr int kFoldRegs = 224;
 // starts 64 rows before the tile, lanes 64..127 get rows 0..63 and the remaining
 // columns, so all four warps build coefficients.
 template <int CMAX> struct EqPlan {
+    static constexpr int NPL = (CMAX + 31) / 32;              // token columns per lane
+    static constexpr bool TAIL = CMAX > 64;                   // K atoms of 64 tokens + 16
+    static constexpr int W_BYTES = 8192 + (TAIL ? 2048 : 0);
     static constexpr int NPA = (CMAX + 16 + 15) & ~15;
     static constexpr int SUBK = NPA * 128;
     static constexpr int SUBV = CMAX * 128;
@@ -94,12 +98,12 @@ template <int CMAX> struct EqPlan {
     static constexpr int BYTES = OFF_S + 128 + 16 * CMAX;
     // TMEM: K.K in [0, CMAX) (then ve, O over it), qe^T in [CMAX, CMAX + 16)
     static constexpr int TMEM_COLS = CMAX + 16 <= 64 ? 64 : 128;
-    static constexpr int BLOCKS_PER_SM = CMAX + 16 <= 64 ? 5 : 3;
-    static_assert(OFF_W % 1024 == 0 && OFF_W + 8192 <= A_END, "W tiles over A and M");
+    static constexpr int BLOCKS_PER_SM = CMAX + 16 <= 64 ? 5 : CMAX <= 64 ? 3 : 2;
+    static_assert(OFF_W % 1024 == 0 && OFF_W + W_BYTES <= A_END, "W tiles over A and M");
     static_assert(OFF_QE >= 32768 && OFF_QE + 8192 <= OFF_S, "qe tile past the quarter buffers");
     static_assert(OFF_K + SUBK + 16384 <= BYTES, "M = 128 operand reads stay inside the allocation");
     static_assert(OFF_K >= 8192, "an operand may start 64 rows before the [K;Q] tile");
-    static_assert(CMAX % 16 == 0 && CMAX <= 64, "token columns: at most two per lane");
+    static_assert(CMAX % 16 == 0 && (CMAX <= 64 || CMAX == 80), "token columns: one 64-token atom, then 16");
     static_assert((SUBK % 1024) == 0 && (OFF_K % 1024) == 0 && (SUBV % 1024) == 0, "swizzle atoms");
 };
 
@@ -232,11 +236,13 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
             bvr[i] = __ldg(reinterpret_cast<const uint4 *>(bv + static_cast<size_t>(r) * 128) + dc);
         }
     }
-    float gq[2] = {0.f, 0.f}, bq[2] = {0.f, 0.f};
+    float gq[P::NPL], bq[P::NPL];
     if (warp == 0) {
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < P::NPL; ++i) {
             const int t = lane + 32 * i;
+            gq[i] = 0.f;
+            bq[i] = 0.f;
             if (t < len) {
                 gq[i] = a.buf_g[unit * cap + t];
                 bq[i] = a.buf_beta[unit * cap + t];
@@ -285,9 +291,9 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
         if (r >= C && r < CMAX) *v_at(r, dc) = make_uint4(0u, 0u, 0u, 0u);
     }
     if (warp == 0) {                                              // compensated scan of g
-        float hi[2], lo[2];
+        float hi[P::NPL], lo[P::NPL];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < P::NPL; ++i) {
             hi[i] = gq[i];
             lo[i] = 0.f;
 #pragma unroll
@@ -301,14 +307,15 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
                 }
             }
         }
-        const float chh = __shfl_sync(0xffffffffu, hi[0], 31), cll = __shfl_sync(0xffffffffu, lo[0], 31);
-        {
-            const float s1 = hi[1] + chh, bp = s1 - hi[1];
-            lo[1] += cll + ((hi[1] - (s1 - bp)) + (chh - bp));
-            hi[1] = s1;
+#pragma unroll
+        for (int i = 1; i < P::NPL; ++i) {                        // carry the earlier columns' total
+            const float chh = __shfl_sync(0xffffffffu, hi[i - 1], 31), cll = __shfl_sync(0xffffffffu, lo[i - 1], 31);
+            const float s1 = hi[i] + chh, bp = s1 - hi[i];
+            lo[i] += cll + ((hi[i] - (s1 - bp)) + (chh - bp));
+            hi[i] = s1;
         }
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < P::NPL; ++i) {
             const int t = lane + 32 * i;
             if (t < CMAX) {                                       // zeros past the last token
                 const bool live = t < C;
@@ -417,44 +424,52 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
     tc_fence_before();                                            // K.K columns are reused by ve and O
     __syncthreads();
     // ---- W = M (I + A)^{-1}: warp w holds draft rows 4w .. 4w + 3, lane l token columns
-    //      l and l + 32; column s is final once every s' > s has been subtracted
-    float x0[4], x1[4];
+    //      l, l + 32 (and l + 64); column s is final once every s' > s has been subtracted
+    float x[P::NPL][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const float *mr = sMm + (4 * warp + i) * CMAX;
-        x0[i] = mr[lane];
-        x1[i] = lane + 32 < CMAX ? mr[lane + 32] : 0.f;
+#pragma unroll
+        for (int j = 0; j < P::NPL; ++j) x[j][i] = lane + 32 * j < CMAX ? mr[lane + 32 * j] : 0.f;
     }
 #pragma unroll 2
     for (int s = C - 1; s >= 0; --s) {
         const float *ar = sAm + s * CMAX;
-        const float a0 = ar[lane], a1 = lane + 32 < CMAX ? ar[lane + 32] : 0.f;
-        const bool upper = s >= 32;
+        float av[P::NPL];
+#pragma unroll
+        for (int j = 0; j < P::NPL; ++j) av[j] = lane + 32 * j < CMAX ? ar[lane + 32 * j] : 0.f;
+        const int seg = s >> 5;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float w = __shfl_sync(0xffffffffu, upper ? x1[i] : x0[i], s & 31);
-            x0[i] = fmaf(-w, a0, x0[i]);
-            x1[i] = fmaf(-w, a1, x1[i]);
+            float xs = x[0][i];
+#pragma unroll
+            for (int j = 1; j < P::NPL; ++j) xs = seg == j ? x[j][i] : xs;
+            const float w = __shfl_sync(0xffffffffu, xs, s & 31);
+#pragma unroll
+            for (int j = 0; j < P::NPL; ++j) x[j][i] = fmaf(-w, av[j], x[j][i]);
         }
     }
     __syncthreads();                                              // A, M no longer read: W goes over them
     // ---- W beta gamma and W beta as K-major [16][64] tiles, each the sum of two bf16
-    //      terms (relative error 2^-16, far below that of the tf32 checkpoint product)
+    //      terms (relative error 2^-16, far below that of the tf32 checkpoint product);
+    //      token columns past 64 in [16][16] tiles with 32-byte swizzle
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    for (int half = 0; half < P::NPL; ++half) {
         const int s = lane + 32 * half;
         if (s < CMAX) {
             const float bs = sBeta[s], bg = bs * sGam[s];
+            const bool tail = P::TAIL && s >= 64;
+            const uint32_t stride = tail ? 512 : 2048;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int t2 = 4 * warp + i;
-                const float w = half ? x1[i] : x0[i];
+                const float w = x[half][i];
                 __nv_bfloat16 t4[4];
                 split2(w * bg, t4[0], t4[1]);
                 split2(w * bs, t4[2], t4[3]);
-                const uint32_t off = sw128(t2, s >> 3) + (s & 7) * 2;
+                const uint32_t off = (tail ? 8192 + sw32(t2, (s - 64) >> 3) : sw128(t2, s >> 3)) + (s & 7) * 2;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) *reinterpret_cast<__nv_bfloat16 *>(sW + j * 2048 + off) = t4[j];
+                for (int j = 0; j < 4; ++j) *reinterpret_cast<__nv_bfloat16 *>(sW + j * stride + off) = t4[j];
             }
         }
     }
@@ -464,15 +479,18 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
         tc_fence_after();
         const uint32_t idQ = idesc_mn(1, 128, 16) | kIdescMnMajorA;
         const int nks = CP / 16;
-        const uint64_t dk = desc_mn_sw128(kq0, P::SUBK), dv = desc_mn_sw128(v0, P::SUBV), dw = desc_sw128(w0);
+        const uint64_t dk = desc_mn_sw128(kq0, P::SUBK), dv = desc_mn_sw128(v0, P::SUBV), dw = desc_sw128(w0),
+                       dwt = desc_sw32(w0 + 8192);
 #pragma unroll
         for (int ks = 0; ks < CMAX / 16; ++ks) {
             if (ks < nks) {
                 const uint64_t ak = desc_add(dk, ks * 2048), av = desc_add(dv, ks * 2048);
 #pragma unroll
                 for (int sp = 0; sp < 2; ++sp) {
-                    mma_bf16(tmem + COL_Q, ak, desc_add(dw, sp * 2048 + ks * 32), idQ, (sp | ks) != 0);
-                    mma_bf16(tmem + COL_V, av, desc_add(dw, (2 + sp) * 2048 + ks * 32), idQ, (sp | ks) != 0);
+                    const uint64_t wq = ks < 4 ? desc_add(dw, sp * 2048 + ks * 32) : desc_add(dwt, sp * 512);
+                    const uint64_t wv = ks < 4 ? desc_add(dw, (2 + sp) * 2048 + ks * 32) : desc_add(dwt, (2 + sp) * 512);
+                    mma_bf16(tmem + COL_Q, ak, wq, idQ, (sp | ks) != 0);
+                    mma_bf16(tmem + COL_V, av, wv, idQ, (sp | ks) != 0);
                 }
             }
         }
@@ -610,7 +628,14 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
 //   [0, 32K) and [OFF_Q, +32K); draft (DRAFT): its token tiles in the fp32 key region
 //   (free once E' is formed) and qe over the value rows (free after the fold)
 //   [OFF_SC, ...)          mbarriers, TMEM slot, flags, G (hi, lo), beta, gamma, D, list
+// CMAX = 80: K K^T is one M = 128 MMA (rows 0..79 in lanes 0..79), and every operand
+// whose K extent is the tokens holds tokens 64..79 in a second, 32-byte swizzled atom:
+// F's at [OFF_KF + OFF_FT, +2 x 80 x 32), R''s at [OFF_KF + OFF_RT, +8K) (both free
+// of the draft tiles), E'^T's at [OFF_ET, +8K) (over Tinv, read once F is formed).
 template <int CMAX> struct FoldPlan {
+    static constexpr bool SPLIT = CMAX <= 64;                 // K K^T rows in 64 lanes, twice
+    static constexpr bool TAIL = CMAX > 64;
+    static constexpr int NPL = (CMAX + 31) / 32;              // tokens per lane of warp 0
     static constexpr int SUBK = CMAX * 128;
     static constexpr int OFF_AT = 0;
     static constexpr int OFF_TI = OFF_AT + CMAX * CMAX * 4;
@@ -625,7 +650,12 @@ template <int CMAX> struct FoldPlan {
     static constexpr int OFF_Q = OFF_KF + 4 * KFSUB;
     static constexpr int OFF_SC = OFF_Q + 32768;
     static constexpr int BYTES = OFF_SC + 160 + 20 * CMAX + 256;
-    static_assert(CMAX == 48 || CMAX == 64, "token blocks");
+    static constexpr int OFF_FT = 2 * CMAX * 128;             // from OFF_KF: F, tokens 64..79
+    static constexpr int OFF_RT = (OFF_FT + 2 * CMAX * 32 + 1023) & ~1023;   // from OFF_KF: R', tokens 64..79
+    static constexpr int OFF_ET = 32768;                      // E'^T, tokens 64..79
+    static_assert(CMAX == 48 || CMAX == 64 || CMAX == 80, "token blocks");
+    static_assert(!TAIL || (OFF_RT >= 22528 && OFF_RT + 8192 <= 4 * KFSUB), "R' tail past the draft tiles");
+    static_assert(!TAIL || (OFF_ET >= OFF_TI && OFF_ET + 8192 <= OFF_V), "E' tail over Tinv, below the values");
     static_assert(OFF_K + SUBK + 16384 <= OFF_SC, "M = 128 operand reads stay inside the allocation");
     static_assert(OFF_K >= 8192 && K_END <= OFF_V, "64 rows of room before the keys; keys below the values");
     static_assert(2 * CMAX * 128 <= 4 * KFSUB, "F over the fp32 key tile");
@@ -680,7 +710,8 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
     float *dGl = dGh + 16;
     float *dBeta = dGl + 16;
     float *dGam = dBeta + 16;
-    constexpr uint32_t COL_KK = 0, COL_E = 64, COL_P = 0, COL_F = 128;
+    // E' is read out before the fold contraction is issued into COL_F
+    constexpr uint32_t COL_KK = 0, COL_E = P::TAIL ? 128 : 64, COL_P = 0, COL_F = 128;
 
     if (tid == 0) {
 #pragma unroll
@@ -753,6 +784,7 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
             const __nv_bfloat16 *bk = reinterpret_cast<const __nv_bfloat16 *>(a.buf_k) + unit * cap * 128;
             const __nv_bfloat16 *bv = reinterpret_cast<const __nv_bfloat16 *>(a.buf_v) + unit * cap * 128;
             constexpr int NV = CMAX * 16 / kThreads;
+            static_assert(NV * kThreads == CMAX * 16, "token rows over the threads");
             uint4 raw[NV], vload[NV];
 #pragma unroll
             for (int i = 0; i < NV; ++i) {
@@ -764,11 +796,13 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                     vload[i] = __ldg(reinterpret_cast<const uint4 *>(bv + static_cast<size_t>(r) * 128) + c);
                 }
             }
-            float gq[2] = {0.f, 0.f}, bq[2] = {0.f, 0.f};
+            float gq[P::NPL], bq[P::NPL];
             if (warp == 0) {
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
+                for (int i = 0; i < P::NPL; ++i) {
                     const int t = lane + 32 * i;
+                    gq[i] = 0.f;
+                    bq[i] = 0.f;
                     if (t < L) {
                         gq[i] = a.buf_g[unit * cap + t];
                         bq[i] = a.buf_beta[unit * cap + t];
@@ -788,9 +822,9 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                 *reinterpret_cast<float4 *>(tile + sw128(r, ch + 1)) = make_float4(fl[4], fl[5], fl[6], fl[7]);
             }
             if (warp == 0) {                                      // compensated scan of g
-                float hi[2], lo[2];
+                float hi[P::NPL], lo[P::NPL];
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
+                for (int i = 0; i < P::NPL; ++i) {
                     hi[i] = gq[i];
                     lo[i] = 0.f;
 #pragma unroll
@@ -804,18 +838,26 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                         }
                     }
                 }
-                const float chh = __shfl_sync(0xffffffffu, hi[0], 31), cll = __shfl_sync(0xffffffffu, lo[0], 31);
-                {
-                    const float s1 = hi[1] + chh, bp = s1 - hi[1];
-                    lo[1] += cll + ((hi[1] - (s1 - bp)) + (chh - bp));
-                    hi[1] = s1;
+#pragma unroll
+                for (int i = 1; i < P::NPL; ++i) {                // carry the earlier tokens' total
+                    const float chh = __shfl_sync(0xffffffffu, hi[i - 1], 31);
+                    const float cll = __shfl_sync(0xffffffffu, lo[i - 1], 31);
+                    const float s1 = hi[i] + chh, bp = s1 - hi[i];
+                    lo[i] += cll + ((hi[i] - (s1 - bp)) + (chh - bp));
+                    hi[i] = s1;
                 }
                 // G_{L-1} (hi, lo) from the lane that holds it
-                const int src = (L - 1) & 31;
-                const float gLh = __shfl_sync(0xffffffffu, (L - 1) >= 32 ? hi[1] : hi[0], src);
-                const float gLl = __shfl_sync(0xffffffffu, (L - 1) >= 32 ? lo[1] : lo[0], src);
+                const int src = (L - 1) & 31, seg = (L - 1) >> 5;
+                float sh = hi[0], sl = lo[0];
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
+                for (int i = 1; i < P::NPL; ++i) {
+                    sh = seg == i ? hi[i] : sh;
+                    sl = seg == i ? lo[i] : sl;
+                }
+                const float gLh = __shfl_sync(0xffffffffu, sh, src);
+                const float gLl = __shfl_sync(0xffffffffu, sl, src);
+#pragma unroll
+                for (int i = 0; i < P::NPL; ++i) {
                     const int t = lane + 32 * i;
                     if (t < CMAX) {
                         const bool live = t < L;
@@ -858,8 +900,9 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
             };
             // K K^T in two column ranges: lanes 0..63 hold rows 0..63 for columns [0, ca),
             // and, from an operand starting 64 rows before the key tile, lanes 64..127
-            // hold rows 0..63 for columns [ca, Lp); all four warps then build A^T
-            const int ca = Lp == 16 ? 16 : ((Lp / 2 + 15) & ~15);
+            // hold rows 0..63 for columns [ca, Lp); all four warps then build A^T.
+            // Beyond 64 tokens: one MMA, lane t = row t, three warps build A^T.
+            const int ca = !P::SPLIT ? Lp : Lp == 16 ? 16 : ((Lp / 2 + 15) & ~15);
             if (tid == 0 && !expire) {                            // K K^T
                 tc_fence_after();
                 const uint32_t idA = idesc_mn(1, 128, ca), idB = idesc_mn(1, 128, Lp - ca);
@@ -869,7 +912,7 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                     const uint64_t d = desc_add(dK, (ks >> 2) * P::SUBK + (ks & 3) * 32);
                     mma_bf16(tmem + COL_KK, d, d, idA, ks > 0);
                 }
-                if (Lp > ca) {
+                if (P::SPLIT && Lp > ca) {
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t off = (ks >> 2) * P::SUBK + (ks & 3) * 32;
@@ -901,11 +944,12 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
             }
             tc_fence_after();
             // ---- A^T: thread t writes column t of A (row t of A^T): A[t][s] for s < t;
-            //      warps 0-1 columns s in [0, ca), warps 2-3 the rest (token t = tid & 63)
-            if ((warp & 1) * 32 < CMAX) {                         // warp-uniform: collective loads
-                const int t = tid & 63;
+            //      warps 0-1 columns s in [0, ca), warps 2-3 the rest (token t = tid & 63);
+            //      beyond 64 tokens, token t = tid over all columns
+            if ((P::SPLIT ? (warp & 1) : warp) * 32 < CMAX) {     // warp-uniform: collective loads
+                const int t = P::SPLIT ? (tid & 63) : tid;
                 const float gh = t < L ? sGh[t] : 0.f, gl = t < L ? sGl[t] : 0.f, bt = t < L ? sBeta[t] : 0.f;
-                const int cbeg = warp < 2 ? 0 : ca, cend = warp < 2 ? ca : CMAX;
+                const int cbeg = (!P::SPLIT || warp < 2) ? 0 : ca, cend = (!P::SPLIT || warp >= 2) ? CMAX : ca;
 #pragma unroll
                 for (int cb = 0; cb < CMAX / 16; ++cb) {
                     const int c0 = cb * 16;
@@ -1038,18 +1082,21 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                         __nv_bfloat16 hh[8], ll[8];
 #pragma unroll
                         for (int j = 0; j < 8; ++j) split2(-gm[j] * pk[8 * hf + j], hh[j], ll[j]);
-                        const uint32_t off = sw128(tid, 2 * cb + hf);
-                        *reinterpret_cast<uint4 *>(sR + off) = make_uint4(
+                        const bool tail = P::TAIL && cb >= 4;         // tokens 64..79
+                        uint8_t *dst = tail ? sKf + P::OFF_RT + sw32(tid, hf) : sR + sw128(tid, 2 * cb + hf);
+                        const uint32_t lo_off = tail ? 4096 : 16384;
+                        *reinterpret_cast<uint4 *>(dst) = make_uint4(
                             pack2(hh[0], hh[1]), pack2(hh[2], hh[3]), pack2(hh[4], hh[5]), pack2(hh[6], hh[7]));
-                        *reinterpret_cast<uint4 *>(sR + 16384 + off) = make_uint4(
+                        *reinterpret_cast<uint4 *>(dst + lo_off) = make_uint4(
                             pack2(ll[0], ll[1]), pack2(ll[2], ll[3]), pack2(ll[4], ll[5]), pack2(ll[6], ll[7]));
                     }
                 }
             }
             // ---- F[s'][s] = beta_s' D_s Tinv[s][s'] as two bf16 K-major tiles [Lp][64] (over
-            //      the fp32 key tile, no longer read)
-            for (int e = tid; e < Lp * 64 / 8; e += kThreads) {
-                const int sp = e >> 3, c8 = e & 7;                // row s', 8 columns s = 8 c8 ..
+            //      the fp32 key tile, no longer read); columns 64..79 in [Lp][16] tiles
+            constexpr int NCH = P::TAIL ? 10 : 8;                 // 8-column chunks per row
+            for (int e = tid; e < Lp * NCH; e += kThreads) {
+                const int sp = e / NCH, c8 = e % NCH;             // row s', 8 columns s = 8 c8 ..
                 const float bsp = sBeta[sp];
                 __nv_bfloat16 hh[8], ll[8];
 #pragma unroll
@@ -1058,10 +1105,12 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                     const float v = s < CMAX ? bsp * sD[s] * sTi[s * CMAX + sp] : 0.f;
                     split2(v, hh[j], ll[j]);
                 }
-                const uint32_t off = sw128(sp, c8);
-                *reinterpret_cast<uint4 *>(sF + off) =
+                const bool tail = P::TAIL && c8 >= 8;
+                uint8_t *dst = tail ? sF + P::OFF_FT + sw32(sp, c8 - 8) : sF + sw128(sp, c8);
+                const uint32_t lo_off = tail ? CMAX * 32 : CMAX * 128;
+                *reinterpret_cast<uint4 *>(dst) =
                     make_uint4(pack2(hh[0], hh[1]), pack2(hh[2], hh[3]), pack2(hh[4], hh[5]), pack2(hh[6], hh[7]));
-                *reinterpret_cast<uint4 *>(sF + CMAX * 128 + off) =
+                *reinterpret_cast<uint4 *>(dst + lo_off) =
                     make_uint4(pack2(ll[0], ll[1]), pack2(ll[2], ll[3]), pack2(ll[4], ll[5]), pack2(ll[6], ll[7]));
             }
             fence_proxy_async();
@@ -1069,12 +1118,15 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
             if (tid == 0) {                                       // E^T = K^T F^T (keys MN-major)
                 tc_fence_after();
                 const uint32_t idE = idesc_mn(1, 128, Lp) | kIdescMnMajorA;
+                const uint64_t dFt = desc_sw32(f0 + P::OFF_FT);
 #pragma unroll
                 for (int ks = 0; ks < CMAX / 16; ++ks) {
                     if (ks < nb) {
                         const uint64_t ak = desc_add(dKmn, ks * 2048);
-                        mma_bf16(tmem + COL_E, ak, desc_add(dF, ks * 32), idE, ks > 0);
-                        mma_bf16(tmem + COL_E, ak, desc_add(dF, CMAX * 128 + ks * 32), idE, 1);
+                        const uint64_t fh = ks < 4 ? desc_add(dF, ks * 32) : dFt;
+                        const uint64_t fl = ks < 4 ? desc_add(dF, CMAX * 128 + ks * 32) : desc_add(dFt, CMAX * 32);
+                        mma_bf16(tmem + COL_E, ak, fh, idE, ks > 0);
+                        mma_bf16(tmem + COL_E, ak, fl, idE, 1);
                     }
                 }
                 mma_commit(&bar[1]);
@@ -1100,10 +1152,12 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                         __nv_bfloat16 hh[8], ll[8];
 #pragma unroll
                         for (int j = 0; j < 8; ++j) split2(ev[8 * hf + j], hh[j], ll[j]);
-                        const uint32_t off = sw128(tid, 2 * cb + hf);
-                        *reinterpret_cast<uint4 *>(sEt + off) = make_uint4(pack2(hh[0], hh[1]), pack2(hh[2], hh[3]),
-                                                                           pack2(hh[4], hh[5]), pack2(hh[6], hh[7]));
-                        *reinterpret_cast<uint4 *>(sEt + 16384 + off) = make_uint4(
+                        const bool tail = P::TAIL && cb >= 4;         // tokens 64..79
+                        uint8_t *dst = tail ? smem_raw + P::OFF_ET + sw32(tid, hf) : sEt + sw128(tid, 2 * cb + hf);
+                        const uint32_t lo_off = tail ? 4096 : 16384;
+                        *reinterpret_cast<uint4 *>(dst) = make_uint4(pack2(hh[0], hh[1]), pack2(hh[2], hh[3]),
+                                                                     pack2(hh[4], hh[5]), pack2(hh[6], hh[7]));
+                        *reinterpret_cast<uint4 *>(dst + lo_off) = make_uint4(
                             pack2(ll[0], ll[1]), pack2(ll[2], ll[3]), pack2(ll[4], ll[5]), pack2(ll[6], ll[7]));
                     }
                 }
@@ -1113,12 +1167,15 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
             if (tid == 0) {                                       // D = V^T E' + R' E'
                 tc_fence_after();
                 const uint32_t idF = idesc_mn(1, 128, 128), idV = idF | kIdescMnMajorA;
+                const uint64_t dRt = desc_sw32(kf0 + P::OFF_RT), dEt = desc_sw32(saddr(smem_raw) + P::OFF_ET);
 #pragma unroll
                 for (int ks = 0; ks < CMAX / 16; ++ks) {
                     if (ks < nb) {
                         const uint64_t av = desc_add(dVmn, ks * 2048);
-                        const uint64_t rh = desc_add(dR, ks * 32), rl = desc_add(dR, 16384 + ks * 32);
-                        const uint64_t eh = desc_add(dE, ks * 32), el = desc_add(dE, 16384 + ks * 32);
+                        const uint64_t rh = ks < 4 ? desc_add(dR, ks * 32) : dRt;
+                        const uint64_t rl = ks < 4 ? desc_add(dR, 16384 + ks * 32) : desc_add(dRt, 4096);
+                        const uint64_t eh = ks < 4 ? desc_add(dE, ks * 32) : dEt;
+                        const uint64_t el = ks < 4 ? desc_add(dE, 16384 + ks * 32) : desc_add(dEt, 4096);
                         mma_bf16(tmem + COL_F, av, eh, idV, ks > 0);
                         mma_bf16(tmem + COL_F, av, el, idV, 1);
                         mma_bf16(tmem + COL_F, rh, eh, idF, 1);
@@ -1429,9 +1486,9 @@ int launch_eq(const gdn_replay_dims *d, const ReplayArgs &a, const CUtensorMap &
 // shared memory; the 224-register cap allows two), at most one per (sequence, head).
 template <bool DRAFT>
 int launch_fold(const gdn_replay_dims *d, const ReplayArgs &a, const CUtensorMap &m, cudaStream_t s) {
-    const bool small = d->cap <= 48;
-    const int smem = small ? FoldPlan<48>::BYTES : FoldPlan<64>::BYTES;
-    auto kern = small ? fold_eq_kernel<48, DRAFT> : fold_eq_kernel<64, DRAFT>;
+    const int smem = d->cap <= 48 ? FoldPlan<48>::BYTES : d->cap <= 64 ? FoldPlan<64>::BYTES : FoldPlan<80>::BYTES;
+    auto kern = d->cap <= 48 ? fold_eq_kernel<48, DRAFT> : d->cap <= 64 ? fold_eq_kernel<64, DRAFT>
+                                                                        : fold_eq_kernel<80, DRAFT>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
         return GDN_ERR_LAUNCH;
@@ -1446,14 +1503,15 @@ int launch_fold(const gdn_replay_dims *d, const ReplayArgs &a, const CUtensorMap
 }  // namespace
 
 bool tc_shape(const gdn_replay_dims *d) {
-    return d->dk == 128 && d->dv == 128 && d->in_dtype == GDN_DTYPE_BF16 && d->T <= 16 && d->cap <= 64;
+    return d->dk == 128 && d->dv == 128 && d->in_dtype == GDN_DTYPE_BF16 && d->T <= 16 && d->cap <= 80;
 }
 
 int tc_verify(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s) {
     if (!tc_shape(d)) return 1;
     CUtensorMap m;
     if (!state_map(&m, a.state_in, d->n_slot * d->H * 128)) return GDN_ERR_LAUNCH;
-    return d->cap <= 48 ? launch_eq<48>(d, a, m, s) : launch_eq<64>(d, a, m, s);
+    return d->cap <= 48 ? launch_eq<48>(d, a, m, s) : d->cap <= 64 ? launch_eq<64>(d, a, m, s)
+                                                                   : launch_eq<80>(d, a, m, s);
 }
 
 int tc_flush(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s) {
@@ -1473,7 +1531,8 @@ int tc_verify_fold(const gdn_replay_dims *d, const ReplayArgs &a, cudaStream_t s
     if (rc) return rc;
     ReplayArgs an = a;                                            // the rest, beside the fold launch
     an.fold_class = 1;
-    return d->cap <= 48 ? launch_eq<48>(d, an, m, s) : launch_eq<64>(d, an, m, s);
+    return d->cap <= 48 ? launch_eq<48>(d, an, m, s) : d->cap <= 64 ? launch_eq<64>(d, an, m, s)
+                                                                    : launch_eq<80>(d, an, m, s);
 }
 
 }  // namespace gdn

@@ -57,7 +57,7 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 constexpr int32_t kStatusTimeout = GDN_STATUS_TIMEOUT;
 
 // Tensor-core path (gdn_replay_tc.cu): d_k = d_v = 128, bf16 inputs, T <= 16,
-// cap <= 64 (tc_shape).  Each returns GDN_OK when it launched, GDN_ERR_LAUNCH when
+// cap <= 80 (tc_shape).  Each returns GDN_OK when it launched, GDN_ERR_LAUNCH when
 // the launch (or the tensor map it needs) failed, and 1 only when the shape is not
 // one it handles (the caller then uses the per-token kernels).
 bool tc_shape(const gdn_replay_dims *d);

@@ -107,6 +107,13 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
            (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
            (static_cast<uint64_t>(2) << 61);
 }
+// K-major, 32-byte swizzle: rows of 32 bytes (16 bf16, one K step), 8-row groups 256
+// bytes apart.  Holds the last 16 columns of an operand whose K extent is 80.
+__device__ __forceinline__ uint64_t desc_sw32(uint32_t addr) {
+    return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(256 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(6) << 61);
+}
 // A descriptor for the same layout `bytes` further on (the start-address field holds
 // address / 16 in 14 bits; shared-memory offsets here stay far below 256 KB).  Issue
 // sequences precompute their base descriptors and add constants: building each
@@ -123,6 +130,11 @@ __host__ __device__ constexpr uint32_t idesc_mn(int fmt, int M, int N) {
 // Byte offset of 16-byte chunk `c` (0..7) of row `r` in a 128B-swizzled tile.
 __device__ __forceinline__ uint32_t sw128(int r, int c) {
     return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+// Byte offset of 16-byte chunk `c` (0..1) of row `r` in a 32B-swizzled tile (address
+// bit 4 XOR bit 7: the two chunks swap in rows 4..7 of every 8-row group).
+__device__ __forceinline__ uint32_t sw32(int r, int c) {
+    return static_cast<uint32_t>(r * 32 + ((c ^ ((r >> 2) & 1)) << 4));
 }
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 &raw, float *f) {

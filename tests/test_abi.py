@@ -47,8 +47,11 @@ def test_kernel_family_query():
     so = lib.load()
     tc = good_dims(T=16, cap=47, threshold=32)
     assert so.gdn_replay_kernel_family(ctypes.byref(tc)) == lib.FAMILY_TCGEN05
+    for cap in (16, 48, 49, 64, 65, 79, 80):                   # the three token-capacity variants
+        d = good_dims(T=16, cap=cap, threshold=1)
+        assert so.gdn_replay_kernel_family(ctypes.byref(d)) == lib.FAMILY_TCGEN05, cap
     for kw in (dict(dk=64, dv=64), dict(in_dtype=lib.DTYPE_F32), dict(T=17, cap=48, threshold=32),
-               dict(cap=65, threshold=32)):
+               dict(cap=81, threshold=32)):
         d = good_dims(**kw)
         assert so.gdn_replay_kernel_family(ctypes.byref(d)) == lib.FAMILY_PERTOKEN, kw
     assert so.gdn_replay_kernel_family(ctypes.byref(good_dims(dk=96))) == -2

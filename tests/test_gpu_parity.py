@@ -361,3 +361,24 @@ def test_short_draft_long_buffer_fused(name):
     pr = Pair(_short_draft(name))
     for s in range(14):
         pr.fused_step(s)
+
+
+# ------------- the per-token kernels at d = 128, bf16 (T = 17 is past the tcgen05 shapes)
+def _t17(name):
+    import dataclasses
+    return dataclasses.replace(WL[name], name=name + "_t17", T=17)
+
+
+@pytest.mark.parametrize("name", ["b8", "edge"])
+def test_pertoken_family_bf16_d128_three_call(name):
+    import speculative_decode_recurrent_gb300 as lib
+    pr = Pair(_t17(name))
+    assert lib.gdn_replay_kernel_family(pr.gd) == lib.FAMILY_PERTOKEN
+    for s in range(8):
+        pr.step(s)
+
+
+def test_pertoken_family_bf16_d128_fused():
+    pr = Pair(_t17("b8"))
+    for s in range(8):
+        pr.fused_step(s)
