@@ -86,32 +86,22 @@ __global__ void __launch_bounds__(kConvThreads) conv_verify_kernel(const ConvArg
     pdl_wait();
     pdl_release();
     if (c0 >= a.D) return;
-    const int slot = a.state_idx ? a.state_idx[b] : b;
-    if (slot < 0 || slot >= a.n_slot) {
-        if (c0 == 0 && t0 == 0) atomicOr(a.status, GDN_STATUS_BAD_SLOT);
-        return;
-    }
-    const int pos = a.ring_pos[slot];
-    if (pos < 0 || pos >= a.cap) {
-        if (c0 == 0 && t0 == 0) atomicOr(a.status, GDN_STATUS_BAD_LEN);
-        return;
-    }
     const int D = a.D, T = a.T, cap = a.cap;
-    TIn *ring = reinterpret_cast<TIn *>(a.ring) + static_cast<size_t>(slot) * cap * D + c0;
     const TIn *x = reinterpret_cast<const TIn *>(a.x) + static_cast<size_t>(b) * T * D + c0;
     TOut *y = reinterpret_cast<TOut *>(a.y) + static_cast<size_t>(b) * T * D + c0;
 
-    // inputs x_{t0-W+1} .. x_{t0-1}, then the chunk
+    // inputs x_{t0-W+1} .. x_{t0-1}, then the chunk.  The draft rows (the chunk, and the
+    // window past the first chunk) do not depend on the ring position: they are in
+    // flight while the slot and the position are read.
     Raw hraw[W > 1 ? W - 1 : 1], xr[kChunk];
-#pragma unroll
-    for (int j = 0; j < W - 1; ++j) {
-        const int u = t0 - (W - 1) + j;
-        const TIn *src = u >= 0 ? x + static_cast<size_t>(u) * D : ring + static_cast<size_t>((pos + u + cap) % cap) * D;
-        hraw[j] = __ldg(reinterpret_cast<const Raw *>(src));
-    }
 #pragma unroll
     for (int u = 0; u < kChunk; ++u) {
         if (t0 + u < T) xr[u] = __ldg(reinterpret_cast<const Raw *>(x + static_cast<size_t>(t0 + u) * D));
+    }
+#pragma unroll
+    for (int j = 0; j < W - 1; ++j) {
+        const int u = t0 - (W - 1) + j;
+        if (u >= 0) hraw[j] = __ldg(reinterpret_cast<const Raw *>(x + static_cast<size_t>(u) * D));
     }
     // the 4 channels' taps: 4 W consecutive floats
     float wt[4 * W], bias[4];
@@ -125,6 +115,22 @@ __global__ void __launch_bounds__(kConvThreads) conv_verify_kernel(const ConvArg
         bias[0] = b4.x; bias[1] = b4.y; bias[2] = b4.z; bias[3] = b4.w;
     } else {
         bias[0] = bias[1] = bias[2] = bias[3] = 0.f;
+    }
+    const int slot = a.state_idx ? a.state_idx[b] : b;
+    if (slot < 0 || slot >= a.n_slot) {
+        if (c0 == 0 && t0 == 0) atomicOr(a.status, GDN_STATUS_BAD_SLOT);
+        return;
+    }
+    const int pos = a.ring_pos[slot];
+    if (pos < 0 || pos >= a.cap) {
+        if (c0 == 0 && t0 == 0) atomicOr(a.status, GDN_STATUS_BAD_LEN);
+        return;
+    }
+    TIn *ring = reinterpret_cast<TIn *>(a.ring) + static_cast<size_t>(slot) * cap * D + c0;
+#pragma unroll
+    for (int j = 0; j < W - 1; ++j) {                    // the committed window (first chunk)
+        const int u = t0 - (W - 1) + j;
+        if (u < 0) hraw[j] = __ldg(reinterpret_cast<const Raw *>(ring + static_cast<size_t>(u + pos + cap) % cap * D));
     }
     float h[W][4];                                       // h[W-1] is the current input
 #pragma unroll

@@ -796,6 +796,37 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                     vload[i] = __ldg(reinterpret_cast<const uint4 *>(bv + static_cast<size_t>(r) * 128) + c);
                 }
             }
+            // DRAFT: the draft rows are requested now, beside the buffered rows, and held in
+            // registers until their tiles are free (after E' is formed)
+            uint4 dkq[DRAFT ? 4 : 1], dvv[DRAFT ? 2 : 1];
+            float dgq = 0.f, dbq = 0.f;
+            if constexpr (DRAFT) {
+                const int T = a.T;
+                const size_t drow0 = (static_cast<size_t>(b) * T * H + h) * 128;
+                const size_t dstride = static_cast<size_t>(H) * 128;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int e = tid + i * kThreads, r = e >> 4, c = e & 15, t = r & 15;
+                    dkq[i] = make_uint4(0u, 0u, 0u, 0u);
+                    if (t < T)
+                        dkq[i] = __ldg(reinterpret_cast<const uint4 *>(
+                                           reinterpret_cast<const __nv_bfloat16 *>(r < 16 ? a.k : a.q) + drow0 +
+                                           static_cast<size_t>(t) * dstride) + c);
+                }
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
+                    dvv[i] = make_uint4(0u, 0u, 0u, 0u);
+                    if (r < T)
+                        dvv[i] = __ldg(reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(a.v) +
+                                                                       drow0 + static_cast<size_t>(r) * dstride) + c);
+                }
+                if (warp == 0 && lane < T) {
+                    const size_t gi = (static_cast<size_t>(b) * T + lane) * H + h;
+                    dgq = a.g[gi];
+                    dbq = a.beta[gi];
+                }
+            }
             float gq[P::NPL], bq[P::NPL];
             if (warp == 0) {
 #pragma unroll
@@ -1202,32 +1233,6 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
             constexpr uint32_t COL_KD = 0, COL_DQ = 16, COL_DV = 32, COL_DO = 48;
             if constexpr (DRAFT) {
                 const int T = a.T;
-                const size_t drow0 = (static_cast<size_t>(b) * T * H + h) * 128;
-                const size_t dstride = static_cast<size_t>(H) * 128;
-                uint4 dkq[4], dvv[2];
-                float dgq = 0.f, dbq = 0.f;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int e = tid + i * kThreads, r = e >> 4, c = e & 15, t = r & 15;
-                    dkq[i] = make_uint4(0u, 0u, 0u, 0u);
-                    if (t < T)
-                        dkq[i] = __ldg(reinterpret_cast<const uint4 *>(
-                                           reinterpret_cast<const __nv_bfloat16 *>(r < 16 ? a.k : a.q) + drow0 +
-                                           static_cast<size_t>(t) * dstride) + c);
-                }
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int e = tid + i * kThreads, r = e >> 4, c = e & 15;
-                    dvv[i] = make_uint4(0u, 0u, 0u, 0u);
-                    if (r < T)
-                        dvv[i] = __ldg(reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(a.v) +
-                                                                       drow0 + static_cast<size_t>(r) * dstride) + c);
-                }
-                if (warp == 0 && lane < T) {
-                    const size_t gi = (static_cast<size_t>(b) * T + lane) * H + h;
-                    dgq = a.g[gi];
-                    dbq = a.beta[gi];
-                }
                 __nv_bfloat16 *wk = reinterpret_cast<__nv_bfloat16 *>(a.buf_k) + unit * cap * 128;
                 __nv_bfloat16 *wv = reinterpret_cast<__nv_bfloat16 *>(a.buf_v) + unit * cap * 128;
 #pragma unroll
