@@ -22,7 +22,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRCS = [os.path.join(_HERE, f) for f in ("gdn_oracle.c", "gdn_layer_ops_oracle.c")]
 _LIB = os.path.join(_HERE, "_build", "libgdnoracle.so")
 
-BAD_ACCEPT, NO_ROOM, BAD_LEN = 1, 2, 4
+BAD_ACCEPT, NO_ROOM, BAD_LEN, BAD_SLOT = 1, 2, 4, 8
 
 
 class _ConvDims(ctypes.Structure):
@@ -63,7 +63,10 @@ def _load():
         lib.orc_verify.argtypes = [ctypes.POINTER(_Dims)] + [P] * 14
         lib.orc_accept.argtypes = [ctypes.POINTER(_Dims), P, P, P, P]
         lib.orc_flush.argtypes = [ctypes.POINTER(_Dims)] + [P] * 7 + [ctypes.c_int, P]
-        for f in (lib.orc_recur, lib.orc_verify, lib.orc_accept, lib.orc_flush):
+        lib.orc_nr_verify.argtypes = [ctypes.POINTER(_Dims)] + [P] * 10
+        lib.orc_nr_accept.argtypes = [ctypes.POINTER(_Dims)] + [P] * 5
+        for f in (lib.orc_recur, lib.orc_verify, lib.orc_accept, lib.orc_flush, lib.orc_nr_verify,
+                  lib.orc_nr_accept):
             f.restype = ctypes.c_int
         CD = ctypes.POINTER(_ConvDims)
         lib.orc_conv_verify.argtypes = [CD] + [P] * 8
@@ -205,6 +208,52 @@ class Layer:
     def flush(self, force: bool = False):
         flush(self.d, self.state, self.state_idx, self.buf_k, self.buf_v, self.buf_g,
               self.buf_beta, self.buf_len, force, self.status)
+
+
+# ------------------------------------------------- non-replay baseline
+def nr_verify(d: Dims, state, state_idx, q, k, v, g, beta, out, snap, status):
+    """The baseline without a buffer: outputs of the draft block from the current
+    state, and the state after every draft token stored (binary32) in
+    snap [B, H, T, dv, dk].  Never writes ``state``."""
+    H = d.H
+    args = [_f64(state, (d.n_slot, H, d.dv, d.dk)),
+            None if state_idx is None else _i32(state_idx, (d.B,)),
+            _f64(q, (d.B, d.T, H, d.dk)), _f64(k, (d.B, d.T, H, d.dk)), _f64(v, (d.B, d.T, H, d.dv)),
+            _f64(g, (d.B, d.T, H)), _f64(beta, (d.B, d.T, H)), _f64(out, (d.B, d.T, H, d.dv)),
+            _f64(snap, (d.B, H, d.T, d.dv, d.dk)), _i32(status, (1,))]
+    return _load().orc_nr_verify(ctypes.byref(d.c()), *[_p(a) for a in args])
+
+
+def nr_accept(d: Dims, state, state_idx, snap, accepted, status):
+    """Restore by copy: state = snap[b, :, p - 1] for p in [1, T]; p = 0 keeps it."""
+    args = [_f64(state, (d.n_slot, d.H, d.dv, d.dk)),
+            None if state_idx is None else _i32(state_idx, (d.B,)),
+            _f64(snap, (d.B, d.H, d.T, d.dv, d.dk)), _i32(accepted, (d.B,)), _i32(status, (1,))]
+    return _load().orc_nr_accept(ctypes.byref(d.c()), *[_p(a) for a in args])
+
+
+class NonReplayLayer:
+    """One layer of the non-replay baseline held by the oracle: the current state
+    and the snapshots of the last verify."""
+
+    def __init__(self, d: Dims, state, state_idx):
+        self.d = d
+        self.state = np.array(state, dtype=np.float64, order="C")          # a copy: the layer owns it
+        self.state_idx = None if state_idx is None else np.array(state_idx, dtype=np.int32, order="C")
+        self.snap = np.zeros((d.B, d.H, d.T, d.dv, d.dk))
+        self.status = np.zeros(1, np.int32)
+
+    def verify(self, blk: dict) -> np.ndarray:
+        d = self.d
+        f = lambda t: np.ascontiguousarray(np.asarray(t, dtype=np.float64))  # noqa: E731
+        out = np.zeros((d.B, d.T, d.H, d.dv))
+        nr_verify(d, self.state, self.state_idx, f(blk["q"]), f(blk["k"]), f(blk["v"]), f(blk["g"]),
+                  f(blk["beta"]), out, self.snap, self.status)
+        return out
+
+    def accept(self, accepted):
+        acc = np.ascontiguousarray(np.asarray(accepted, dtype=np.int32))
+        nr_accept(self.d, self.state, self.state_idx, self.snap, acc, self.status)
 
 
 # ------------------------------------------------- causal convolution with rollback

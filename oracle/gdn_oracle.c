@@ -243,3 +243,75 @@ int orc_flush(const orc_dims *d, double *state, const int32_t *state_idx,
     free(lens);
     return 0;
 }
+
+/* ------------------------------------------------- non-replay baseline
+ * The data movement ReplaySSM avoids ("The inference stack behind OCRia",
+ * section "Making speculative verification cheaper": restoring a recurrent
+ * state after a rejection moves a lot of data).  Without a buffer the state is
+ * always current; so that a rejection can go back to the state after the
+ * accepted prefix, the verify stores the state after every draft token, and
+ * the accept copies the snapshot of the accepted prefix over the state.
+ *
+ * layouts: state [n_slot, H, dv, dk]; snap [B, H, T, dv, dk] (per batch row,
+ * stored as binary32 like the checkpoint); draft inputs and out as above.
+ * Status: a slot outside [0, n_slot) sets ORC_BAD_SLOT and skips the row; an
+ * accepted count outside [0, T] sets ORC_BAD_ACCEPT and skips the row. */
+#define ORC_BAD_SLOT 8
+
+typedef struct {
+    const orc_dims *d;
+    const double *state; const int32_t *state_idx;
+    const double *q, *k, *v, *g, *beta;
+    double *out, *snap; const unsigned char *skip;
+} nr_verify_ctx;
+
+static void nr_verify_unit(void *p, int b, int h) {
+    nr_verify_ctx *c = (nr_verify_ctx *)p;
+    const orc_dims *d = c->d;
+    if (c->skip[b]) return;
+    const int slot = slot_of(c->state_idx, b);
+    const size_t n = (size_t)d->dv * d->dk;
+    double *S = (double *)malloc(n * sizeof(double));
+    memcpy(S, c->state + st_off(d, slot, h), n * sizeof(double));   /* the state is only read */
+    const long tk = (long)d->H * d->dk, tv = (long)d->H * d->dv, tg = d->H;
+    for (int t = 0; t < d->T; ++t) {
+        orc_recur(d, S, 1,
+                  c->k + dk_off(d, b, t, h), tk, c->v + dv_off(d, b, t, h), tv,
+                  c->g + dg_off(d, b, t, h), c->beta + dg_off(d, b, t, h), tg,
+                  c->q + dk_off(d, b, t, h), tk, c->out + dv_off(d, b, t, h), tv);
+        double *dst = c->snap + (((size_t)b * d->H + h) * d->T + t) * n;
+        for (size_t e = 0; e < n; ++e) dst[e] = (double)(float)S[e];   /* stored as binary32 */
+    }
+    free(S);
+}
+
+int orc_nr_verify(const orc_dims *d, const double *state, const int32_t *state_idx,
+                  const double *q, const double *k, const double *v, const double *g, const double *beta,
+                  double *out, double *snap, int32_t *status)
+{
+    unsigned char *skip = (unsigned char *)calloc(d->B > 0 ? d->B : 1, 1);
+    for (int b = 0; b < d->B; ++b) {
+        const int slot = slot_of(state_idx, b);
+        if (slot < 0 || slot >= d->n_slot) { *status |= ORC_BAD_SLOT; skip[b] = 1; }
+    }
+    nr_verify_ctx c = {d, state, state_idx, q, k, v, g, beta, out, snap, skip};
+    for_each_unit(d, nr_verify_unit, &c);
+    free(skip);
+    return 0;
+}
+
+int orc_nr_accept(const orc_dims *d, double *state, const int32_t *state_idx, const double *snap,
+                  const int32_t *accepted, int32_t *status)
+{
+    const size_t n = (size_t)d->dv * d->dk;
+    for (int b = 0; b < d->B; ++b) {
+        const int slot = slot_of(state_idx, b), p = accepted[b];
+        if (slot < 0 || slot >= d->n_slot) { *status |= ORC_BAD_SLOT; continue; }
+        if (p < 0 || p > d->T) { *status |= ORC_BAD_ACCEPT; continue; }
+        if (p == 0) continue;                     /* everything rejected: the state stays */
+        for (int h = 0; h < d->H; ++h)
+            memcpy(state + st_off(d, slot, h), snap + (((size_t)b * d->H + h) * d->T + (p - 1)) * n,
+                   n * sizeof(double));
+    }
+    return 0;
+}
