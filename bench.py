@@ -577,6 +577,49 @@ def run_extras(args, peak):
                                 "hbm_frac": round(gbs / peak, 4),
                                 "l2": f"cold: {n_sets} input sets rotate (more than twice L2)",
                                 "workload": f"{nw.rows} rows of d={nw.d} (B=32, T=16, H=16), bf16 gate"}
+    # the non-replay baseline on a decode24 layer: the state after every draft token
+    # stored, restored by copy (what checkpoint + buffer replay avoids)
+    wl = synth.WORKLOADS["decode24"]
+    nd = Dims(B=wl.B, H=wl.H, dk=wl.dk, dv=wl.dv, T=wl.T, cap=wl.T, threshold=1, n_slot=wl.n_slot,
+              in_dtype=lib.DTYPE_BF16, scale=wl.scale)
+    n_layers = 4                                          # 4 x 42 MB states; the snapshots alone are 537 MB
+    snap = torch.empty(wl.B * wl.H * wl.T * wl.dv * wl.dk, dtype=torch.float32, device=dev)
+    inits = [synth.initial_layer(wl, l) for l in range(n_layers)]
+    nls = [lib.NonReplayLayer(nd, init["state"], init["state_idx"], dev, snap=snap) for init in inits]
+    nblocks = [[{n: t.to(dev) for n, t in synth.draft_block(wl, l, s).items()} for s in range(DRAFT_POOL)]
+               for l in range(n_layers)]
+    naccs = [[synth.workloads.accepted_counts(wl, l, 1000 + j) for j in range(ACCEPT_PERIOD)]
+             for l in range(n_layers)]
+    nacc_dev = [[a.to(dev) for a in al] for al in naccs]
+    o = torch.empty(wl.B, wl.T, wl.H, wl.dv, device=dev)
+
+    def nr_step(i):
+        s, l = divmod(i, n_layers)
+        b = nblocks[l][s % DRAFT_POOL]
+        nls[l].verify(b["q"], b["k"], b["v"], b["g"], b["beta"], o)
+        nls[l].accept(nacc_dev[l][s % ACCEPT_PERIOD])
+    n = 4 * n_layers
+    t = _graph_total_ms(nr_step, n) / n
+    unit = wl.dv * wl.dk * 4
+    draft = wl.B * wl.T * wl.H * (2 * wl.dk * 2 + wl.dv * 2 + 8)
+    tot = 0
+    for i in range(n):
+        s, l = divmod(i, n_layers)
+        restored = int((naccs[l][s % ACCEPT_PERIOD] > 0).sum()) * wl.H
+        tot += (wl.B * wl.H * unit * (1 + wl.T) + draft + wl.B * wl.T * wl.H * wl.dv * 4
+                + 2 * restored * unit)
+    for x in nls:
+        if int(x.status.item()) != 0:
+            raise RuntimeError(f"non-replay status {int(x.status.item())}")
+    gbs = tot / n / (t * 1e-3) / 1e9
+    out["nonreplay"] = {"us_per_layer_step": round(t * 1000, 3), "algorithmic_bytes_per_step": int(tot / n),
+                        "hbm_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4),
+                        "kernels": "nonreplay_verify (CUDA cores, snapshot stream) + nonreplay_accept (copy)",
+                        "l2": "the 537 MB of snapshots per step exceed L2; 4 layers' states rotate",
+                        "timing": "verify + accept steps back to back in one captured graph",
+                        "workload": f"decode24 layer without a buffer: B={wl.B}, H={wl.H}, d={wl.dk}, "
+                                    f"T={wl.T}, every draft token's state stored"}
+    del nls, snap
     torch.cuda.synchronize()
     return out
 
@@ -679,6 +722,9 @@ def main():
                       "three_call": "gdn_replay_verify + gdn_replay_accept + gdn_replay_flush per layer, "
                                     "one stream"}
         extras = None if args.no_extras else run_extras(args, peak)
+        if extras and "nonreplay" in extras:              # what replay saves on the same layer shape
+            extras["nonreplay"]["over_headline"] = round(extras["nonreplay"]["us_per_layer_step"] /
+                                                         s_h["us_per_layer"], 2)
         import speculative_decode_recurrent_gb300 as lib
         hd = lib.Dims(B=wl.B, H=wl.H, dk=wl.dk, dv=wl.dv, T=wl.T, cap=wl.cap, threshold=wl.threshold,
                       n_slot=wl.n_slot, in_dtype=lib.DTYPE_BF16, scale=wl.scale)

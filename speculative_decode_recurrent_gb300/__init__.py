@@ -21,7 +21,8 @@ __all__ = ["Dims", "GdnError", "load", "gdn_replay_verify", "gdn_replay_accept",
            "STATUS_NO_ROOM", "STATUS_BAD_LEN", "STATUS_BAD_SLOT", "STATUS_TIMEOUT",
            "STATUS_DRAIN", "FLAG_TEST_EXPIRE", "FAMILY_TCGEN05", "FAMILY_PERTOKEN", "DTYPE_BF16",
            "DTYPE_F32", "ReplayLayer", "ConvDims", "gdn_conv_verify", "gdn_conv_accept",
-           "gdn_gated_rmsnorm_fp8", "ConvLayer", "CONV_ACT_NONE", "CONV_ACT_SILU"]
+           "gdn_gated_rmsnorm_fp8", "ConvLayer", "CONV_ACT_NONE", "CONV_ACT_SILU",
+           "gdn_nonreplay_verify", "gdn_nonreplay_accept", "NonReplayLayer"]
 
 DTYPE_BF16, DTYPE_F32 = 0, 1
 STATUS_BAD_ACCEPT, STATUS_NO_ROOM, STATUS_BAD_LEN, STATUS_BAD_SLOT, STATUS_TIMEOUT = 1, 2, 4, 8, 16
@@ -86,7 +87,10 @@ def load(rebuild: bool = False) -> ctypes.CDLL:
         lib.gdn_conv_verify.argtypes = [CD] + [P] * 9
         lib.gdn_conv_accept.argtypes = [CD, P, P, P, P, P]
         lib.gdn_gated_rmsnorm_fp8.argtypes = [I, I, P, P, I, P, ctypes.c_float, ctypes.c_float, P, P]
-        for f in (lib.gdn_conv_verify, lib.gdn_conv_accept, lib.gdn_gated_rmsnorm_fp8):
+        lib.gdn_nonreplay_verify.argtypes = [D] + [P] * 11
+        lib.gdn_nonreplay_accept.argtypes = [D] + [P] * 6
+        for f in (lib.gdn_conv_verify, lib.gdn_conv_accept, lib.gdn_gated_rmsnorm_fp8,
+                  lib.gdn_nonreplay_verify, lib.gdn_nonreplay_accept):
             f.restype = ctypes.c_int
         for f in (lib.gdn_replay_verify, lib.gdn_replay_accept, lib.gdn_replay_flush,
                   lib.gdn_replay_verify_fold, lib.gdn_replay_accept_fold, lib.gdn_replay_version,
@@ -253,6 +257,65 @@ class ReplayLayer:
     def accept_fold(self, accepted, stream=None):
         gdn_replay_accept_fold(self.d, self.t["buf_len"], self.t["state_idx"], accepted,
                                self.status, stream)
+
+
+# ---------------------------------------------------------- non-replay baseline
+def _check_nr_sizes(d: Dims, **tensors):
+    B, H, dk, dv, T, n = d.B, d.H, d.dk, d.dv, d.T, d.n_slot
+    need = {"state": n * H * dv * dk, "state_idx": B, "q": B * T * H * dk, "k": B * T * H * dk,
+            "v": B * T * H * dv, "g": B * T * H, "beta": B * T * H, "out": B * T * H * dv,
+            "snap": B * H * T * dv * dk, "accepted": B, "status": 1}
+    for name, t in tensors.items():
+        if isinstance(t, torch.Tensor) and t.numel() < need[name]:
+            raise ValueError(f"{name}: needs at least {need[name]} elements for {d}, got {t.numel()}")
+
+
+def gdn_nonreplay_verify(d: Dims, state, state_idx, q, k, v, g, beta, out, snap, status, stream=None):
+    """The baseline without a buffer (include/gdnnonreplay.h): outputs of the draft
+    block from the current state and the state after every draft token in ``snap``."""
+    tin = _TORCH_IN.get(d.in_dtype)
+    f32, i32 = torch.float32, torch.int32
+    _check_nr_sizes(d, state=state, state_idx=state_idx, q=q, k=k, v=v, g=g, beta=beta, out=out,
+                    snap=snap, status=status)
+    rc = load().gdn_nonreplay_verify(
+        ctypes.byref(d), _ptr(state, f32, "state"), _ptr(state_idx, i32, "state_idx"),
+        _ptr(q, tin, "q"), _ptr(k, tin, "k"), _ptr(v, tin, "v"), _ptr(g, f32, "g"),
+        _ptr(beta, f32, "beta"), _ptr(out, f32, "out"), _ptr(snap, f32, "snap"),
+        _ptr(status, i32, "status"), _stream(stream))
+    _check("gdn_nonreplay_verify", rc)
+
+
+def gdn_nonreplay_accept(d: Dims, state, state_idx, snap, accepted, status, stream=None):
+    """Restore by copy: the state after the accepted prefix (snapshot p - 1)."""
+    f32, i32 = torch.float32, torch.int32
+    _check_nr_sizes(d, state=state, state_idx=state_idx, snap=snap, accepted=accepted, status=status)
+    rc = load().gdn_nonreplay_accept(
+        ctypes.byref(d), _ptr(state, f32, "state"), _ptr(state_idx, i32, "state_idx"),
+        _ptr(snap, f32, "snap"), _ptr(accepted, i32, "accepted"), _ptr(status, i32, "status"),
+        _stream(stream))
+    _check("gdn_nonreplay_accept", rc)
+
+
+class NonReplayLayer:
+    """Device-resident state of one GDN layer under the non-replay baseline, with
+    the snapshot area its verify writes (B x H x T states).  ``snap`` may be shared
+    between layers that are stepped one after the other."""
+
+    def __init__(self, dims: Dims, state, state_idx, device="cuda", snap=None):
+        self.d = dims
+        self.state = state.to(device).contiguous()
+        self.state_idx = None if state_idx is None else state_idx.to(device).contiguous()
+        n = dims.B * dims.H * dims.T * dims.dv * dims.dk
+        self.snap = torch.empty(n, dtype=torch.float32, device=device) if snap is None else snap
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def verify(self, q, k, v, g, beta, out, stream=None):
+        gdn_nonreplay_verify(self.d, self.state, self.state_idx, q, k, v, g, beta, out, self.snap,
+                             self.status, stream)
+
+    def accept(self, accepted, stream=None):
+        gdn_nonreplay_accept(self.d, self.state, self.state_idx, self.snap, accepted, self.status,
+                             stream)
 
 
 # ------------------------------------------------ causal convolution with rollback

@@ -12,8 +12,10 @@ import sys
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SOURCES = [os.path.join(PKG, "csrc", f) for f in ("gdn_replay.cu", "gdn_replay_tc.cu", "gdn_layer_ops.cu")]
+SOURCES = [os.path.join(PKG, "csrc", f)
+           for f in ("gdn_replay.cu", "gdn_replay_tc.cu", "gdn_layer_ops.cu", "gdn_nonreplay.cu")]
 HEADERS = [os.path.join(ROOT, "include", "gdnreplay.h"), os.path.join(ROOT, "include", "gdnlayer.h"),
+           os.path.join(ROOT, "include", "gdnnonreplay.h"),
            os.path.join(PKG, "csrc", "replay_common.h"), os.path.join(PKG, "csrc", "tc_common.cuh")]
 LIB = os.path.join(PKG, "_build", "libgdnreplay.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

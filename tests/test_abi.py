@@ -202,3 +202,43 @@ def test_norm_bad_arguments_rejected_before_launch():
     null_q = list(args); null_q[6] = None
     assert so.gdn_gated_rmsnorm_fp8(4, 128, *null_q) == -1
     assert so.gdn_gated_rmsnorm_fp8(0, 128, *([None] * 2), 0, None, 1e-6, 1.0, None, None) == 0
+
+
+# ---------------------------------------------------------- non-replay baseline
+def test_nonreplay_host_validation():
+    so = lib.load()
+    d = good_dims(T=16, cap=16, threshold=1)
+    assert so.gdn_nonreplay_verify(None, *([FAKE] * 10), None) == -1
+    for i in (0, 2, 3, 4, 5, 6, 7, 8, 9):                       # state_idx (1) may be NULL
+        args = [FAKE] * 10
+        args[i] = None
+        assert so.gdn_nonreplay_verify(ctypes.byref(d), *args, None) == -1, i
+    for i in (0, 2, 3, 4):
+        args = [FAKE] * 5
+        args[i] = None
+        assert so.gdn_nonreplay_accept(ctypes.byref(d), *args, None) == -1, i
+    for kw, code in ((dict(dk=96), -2), (dict(T=65, cap=65), -2), (dict(in_dtype=7), -3),
+                     (dict(flags=1), -2), (dict(H=0), -2), (dict(n_slot=-1), -2)):
+        bad = good_dims(**{**dict(T=16, cap=16, threshold=1), **kw})
+        assert so.gdn_nonreplay_verify(ctypes.byref(bad), *([FAKE] * 10), None) == code, kw
+        assert so.gdn_nonreplay_accept(ctypes.byref(bad), *([FAKE] * 5), None) == code, kw
+    few = good_dims(T=16, cap=16, threshold=1, n_slot=1)       # fewer slots than rows, no slot map
+    args = [FAKE] * 10
+    args[1] = None
+    assert so.gdn_nonreplay_verify(ctypes.byref(few), *args, None) == -2
+    assert so.gdn_nonreplay_accept(ctypes.byref(few), FAKE, None, FAKE, FAKE, FAKE, None) == -2
+    args = [FAKE] * 10
+    args[8] = ctypes.c_void_p(0x10008)                          # snap must be 16-byte aligned
+    assert so.gdn_nonreplay_verify(ctypes.byref(d), *args, None) == -2
+    e = good_dims(B=0, n_slot=0, T=16, cap=16, threshold=1)
+    assert so.gdn_nonreplay_verify(ctypes.byref(e), *([None] * 10), None) == 0
+    assert so.gdn_nonreplay_accept(ctypes.byref(e), *([None] * 5), None) == 0
+
+
+def test_nonreplay_binding_rejects_undersized_snapshots():
+    import torch
+    d = good_dims(T=4, cap=4, threshold=1)
+    small = torch.empty(10, dtype=torch.float32)
+    with pytest.raises(ValueError, match="snap"):
+        lib.gdn_nonreplay_accept(d, torch.empty(2 * 2 * 128 * 128), None, small,
+                                 torch.zeros(2, dtype=torch.int32), torch.zeros(1, dtype=torch.int32))
