@@ -59,6 +59,33 @@ int gdn_nonreplay_verify(const gdn_replay_dims *dims, const float *state, const 
 int gdn_nonreplay_accept(const gdn_replay_dims *dims, float *state, const int32_t *state_idx,
                          const float *snap, const int32_t *accepted, int32_t *status, cudaStream_t stream);
 
+/* Size of the snapshot area inside the library that gdn_nonreplay_step_static uses:
+ * it serves steps with B * H * T * d_v * d_k * 4 <= this many bytes (e.g. 512 snapshots
+ * at d = 128: B = 2, H = 16, T = 16).  Every GPU that loads the library holds it until
+ * the process exits. */
+#define GDN_NONREPLAY_STATIC_SNAP_BYTES (32u << 20)
+
+/* One baseline step (gdn_nonreplay_verify, then gdn_nonreplay_accept) that allocates
+ * nothing: the snapshots go to a fixed area inside the library instead of a caller
+ * buffer.  The paper has no counterpart; this exists for callers that can pass tensors
+ * but cannot call cudaMalloc -- a plugin inside a serving engine whose device memory is
+ * reserved up front by the engine's own allocator and offers the plugin no allocation
+ * hook, or a latency-bound loop where cudaMalloc's implicit device synchronisation is
+ * not allowed.  Inputs and outputs are those of the two calls it replaces: state
+ * (updated in place), state_idx, q, k, v, g, beta, accepted, out, status.
+ *
+ * A step larger than GDN_NONREPLAY_STATIC_SNAP_BYTES of snapshots returns GDN_ERR_DIMS
+ * before anything is launched.  The first call on each device looks up the area's
+ * device address (set-up, once per device, with that device current); make that first
+ * call before any stream capture.  Every call shares the one area and leaves its
+ * snapshots there; nothing in it needs clearing (the verify writes every snapshot the
+ * accept reads), but calls whose work overlaps on the GPU -- on different streams, or
+ * from different threads -- race on it and must be serialised by the caller. */
+int gdn_nonreplay_step_static(const gdn_replay_dims *dims, float *state, const int32_t *state_idx,
+                              const void *q, const void *k, const void *v, const float *g,
+                              const float *beta, const int32_t *accepted, float *out, int32_t *status,
+                              cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

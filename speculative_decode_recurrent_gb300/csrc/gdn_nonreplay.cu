@@ -14,6 +14,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "gdnnonreplay.h"
 #include "replay_common.h"
 
@@ -208,4 +210,50 @@ extern "C" int gdn_nonreplay_accept(const gdn_replay_dims *dims, float *state, c
                 dims->B, dims->H, dims->T, dims->dv, dims->n_slot, dims->scale};
     return launch_pdl(nonreplay_accept_kernel, dim3(dims->H, dims->B), dim3(kCopyThreads), 0, stream, a,
                       dims->dk) == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------------------
+// The baseline step for callers that cannot allocate device memory: the snapshots
+// live in this fixed area (GDN_NONREPLAY_STATIC_SNAP_BYTES) instead of a caller
+// buffer.  Host code must not hand the array's name to a kernel -- on the host it is
+// only a stand-in for the symbol -- so its device address is looked up once per device.
+static __device__ __align__(256) float g_static_snap[GDN_NONREPLAY_STATIC_SNAP_BYTES / sizeof(float)];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_snap_mu;
+float *g_static_snap_dev[kMaxDevices] = {};
+
+// Device address of g_static_snap on the current device (set-up on the first call).
+int static_snap_address(float **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_LAUNCH;
+    std::lock_guard<std::mutex> lock(g_static_snap_mu);
+    if (!g_static_snap_dev[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_snap) != cudaSuccess || !p) return GDN_ERR_LAUNCH;
+        g_static_snap_dev[dev] = static_cast<float *>(p);
+    }
+    *out = g_static_snap_dev[dev];
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" int gdn_nonreplay_step_static(const gdn_replay_dims *dims, float *state, const int32_t *state_idx,
+                                         const void *q, const void *k, const void *v, const float *g,
+                                         const float *beta, const int32_t *accepted, float *out,
+                                         int32_t *status, cudaStream_t stream) {
+    int rc = check_nr(dims, state_idx);
+    if (rc) return rc;
+    if (dims->B == 0) return GDN_OK;
+    if (!state || !q || !k || !v || !g || !beta || !accepted || !out || !status) return GDN_ERR_NULL;
+    const size_t need = static_cast<size_t>(dims->B) * dims->H * dims->T * dims->dv * dims->dk * sizeof(float);
+    if (need > GDN_NONREPLAY_STATIC_SNAP_BYTES) return GDN_ERR_DIMS;
+    float *snap = nullptr;
+    if ((rc = static_snap_address(&snap)) != GDN_OK) return rc;
+    if ((rc = gdn_nonreplay_verify(dims, state, state_idx, q, k, v, g, beta, out, snap, status, stream)) != GDN_OK)
+        return rc;
+    return gdn_nonreplay_accept(dims, state, state_idx, snap, accepted, status, stream);
 }
