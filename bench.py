@@ -45,9 +45,9 @@ FALLBACK_HBM_GBS = 6800.0
 # dram read+write bytes per verify launch from the ncu capture summarised in
 # profiles/; valid only for the kernel source whose hash is recorded with it.
 NCU_TRAFFIC = {         # {(step mode, source_sha1): dram read + write bytes per launch}
-    ("overlap", "9ea9cf214077843edbf01d66ef639cf17c6e85df"): 43.31e6,      # verify_eq_kernel, launch list of profiles/
-    ("three_call", "9ea9cf214077843edbf01d66ef639cf17c6e85df"): 43.30e6,   # verify_eq_kernel, launch list of profiles/
-    ("fused", "9ea9cf214077843edbf01d66ef639cf17c6e85df"): 48.01e6,        # fold launch 14.05 MB + verify launch 33.96 MB
+    ("overlap", "d270b9fc1e0d511a2f37ceacdea6beeb05a9343c"): 43.33e6,      # verify_eq_kernel<48>, profiles/verify_dram_decode24.md
+    ("three_call", "d270b9fc1e0d511a2f37ceacdea6beeb05a9343c"): 43.33e6,   # verify_eq_kernel<48>, same capture
+    ("fused", "d270b9fc1e0d511a2f37ceacdea6beeb05a9343c"): 48.93e6,        # fold launch 16.52 MB + verify launch 32.41 MB
 }
 
 
