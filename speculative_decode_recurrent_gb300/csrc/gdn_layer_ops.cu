@@ -23,7 +23,7 @@ using gdn::pdl_wait;
 
 constexpr int kConvThreads = 128;
 constexpr int kTaps = 4;            // widest kernel
-constexpr int kChunk = 8;           // draft positions per thread
+constexpr int kChunk = 4;           // draft positions per thread (8: 4 % slower, 2: 15 % slower)
 
 struct ConvArgs {
     void *ring;
@@ -75,8 +75,9 @@ __device__ __forceinline__ void store_out4<float>(float *dst, const float (&v)[4
 // otherwise) and the chunk's draft inputs, all requested before the first is used,
 // emits the outputs and stages its raw draft inputs in the ring.  Staged positions
 // pos .. pos+T-1 never meet the window pos-W+1 .. pos-1 (cap >= W - 1 + T), and no two
-// threads write the same bytes, so no barrier is needed.  About 60 registers: the
-// whole grid is resident at once.
+// threads write the same bytes, so no barrier is needed.  64 registers at W = 4 with
+// bf16 rows: eight CTAs per SM, so the decode shape's 1536 CTAs run in about 1.3 waves
+// (chunks of 8 positions fit in one wave but keep fewer loads in flight: 4 % slower).
 template <typename TIn, typename TOut, int W>
 __global__ void __launch_bounds__(kConvThreads) conv_verify_kernel(const ConvArgs a)
 {
