@@ -83,6 +83,34 @@ def test_decode24_all_64_steps(layer, form):
     _LOG[name + "_folds_per_sequence"] = [int(folds.min()), int(folds.max())]
 
 
+@pytest.mark.parametrize("form", ["three_call", "fused"])
+def test_edge_48_steps_long_buffers(form):
+    """The threshold-64 mix (buffers of up to 79 tokens: the 80-token variants of both
+    tensor-core kernels, tokens 64..79 in the second K atom), with extreme gates and
+    the forced accepted counts, for 48 steps: every sequence folds several times."""
+    wl = WL["edge"]
+    pr = Pair(wl)
+    name = f"edge_{form}"
+    DRIFT.clear()
+    idx = pr.gpu.t["state_idx"].long()
+    folds = np.zeros(wl.B, np.int64)
+    longest = 0
+    for s in range(48):
+        before = pr.gpu.t["buf_len"][idx].cpu().numpy()
+        longest = max(longest, int(before.max()))
+        if form == "three_call":
+            pr.step(s)
+            after = pr.gpu.t["buf_len"][idx].cpu().numpy()
+            folds += after < before + pr.block(s)["accepted"].numpy()
+        else:
+            pr.fused_step(s)
+            folds += before >= wl.threshold
+        _record(name, s)
+    assert folds.min() >= 3, folds
+    assert longest + wl.T > 64, longest          # verifies over more than 64 tokens happened
+    _LOG[name + "_folds_per_sequence"] = [int(folds.min()), int(folds.max())]
+
+
 def test_overlapped_schedule_in_a_graph_matches_oracle():
     """The benchmark's headline schedule, replayed from one captured graph per step
     on three decode24 layers: every layer's outputs, state, lengths and buffer bytes
