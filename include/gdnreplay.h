@@ -77,8 +77,12 @@ typedef struct CUstream_st *cudaStream_t;
 #define GDN_STATUS_BAD_SLOT   8   /* state_idx[b] outside [0, n_slot); b skipped */
 #define GDN_STATUS_TIMEOUT   16   /* a bounded on-chip wait expired; the (b, h) unit was skipped.
                                      While this bit is set in *status, gdn_replay_flush and
-                                     gdn_replay_accept_fold reset no buffer length (so no
-                                     buffered token is dropped without being folded) */
+                                     gdn_replay_accept_fold reset no buffer length, so the
+                                     buffer of a unit whose fold gave up is kept.  The units
+                                     folded by the same call then hold their new checkpoint
+                                     and still their buffer length: after a TIMEOUT in a flush
+                                     or a fused step, restore the layer (checkpoint, buffer,
+                                     lengths) from a saved copy before the next verify */
 #define GDN_STATUS_DRAIN     32   /* after an expired wait, the wait for that unit's own copies and
                                      tensor-core operations expired too; its tensor memory was
                                      released anyway (a kernel never hangs), so no result of the
