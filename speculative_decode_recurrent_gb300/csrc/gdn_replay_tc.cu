@@ -432,21 +432,25 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
 #pragma unroll
         for (int j = 0; j < P::NPL; ++j) x[j][i] = lane + 32 * j < CMAX ? mr[lane + 32 * j] : 0.f;
     }
+    // step s changes only the columns below s (A is strictly lower), so a step in token
+    // group seg (columns 32 seg .. 32 seg + 31) updates the column groups 0 .. seg; the
+    // stage is issue-bound with four CTAs on an SM, and the skipped updates were FMAs with
+    // a zero A entry
+#pragma unroll
+    for (int seg = P::NPL - 1; seg >= 0; --seg) {
+        const int s_top = (C < 32 * (seg + 1) ? C : 32 * (seg + 1)) - 1;
 #pragma unroll 2
-    for (int s = C - 1; s >= 0; --s) {
-        const float *ar = sAm + s * CMAX;
-        float av[P::NPL];
+        for (int s = s_top; s >= 32 * seg; --s) {
+            const float *ar = sAm + s * CMAX;
+            float av[P::NPL];
 #pragma unroll
-        for (int j = 0; j < P::NPL; ++j) av[j] = lane + 32 * j < CMAX ? ar[lane + 32 * j] : 0.f;
-        const int seg = s >> 5;
+            for (int j = 0; j <= seg; ++j) av[j] = lane + 32 * j < CMAX ? ar[lane + 32 * j] : 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float xs = x[0][i];
+            for (int i = 0; i < 4; ++i) {
+                const float w = __shfl_sync(0xffffffffu, x[seg][i], s & 31);
 #pragma unroll
-            for (int j = 1; j < P::NPL; ++j) xs = seg == j ? x[j][i] : xs;
-            const float w = __shfl_sync(0xffffffffu, xs, s & 31);
-#pragma unroll
-            for (int j = 0; j < P::NPL; ++j) x[j][i] = fmaf(-w, av[j], x[j][i]);
+                for (int j = 0; j <= seg; ++j) x[j][i] = fmaf(-w, av[j], x[j][i]);
+            }
         }
     }
     __syncthreads();                                              // A, M no longer read: W goes over them

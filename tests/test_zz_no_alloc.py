@@ -38,9 +38,9 @@ def _p(t):
 def test_static_step_matches_the_allocating_calls_twice_in_a_row():
     import speculative_decode_recurrent_gb300 as lib
     so = lib.load()
-    wl = dataclasses.replace(synth.WORKLOADS["b8"], name="b8_static", B=2, H=16)   # 16 MiB of snapshots
+    wl = dataclasses.replace(synth.WORKLOADS["b8"], name="b8_static", B=2, H=16)   # 32 MiB: the whole area
     d = _dims(lib, wl)
-    assert wl.B * wl.H * wl.T * wl.dv * wl.dk * 4 <= 32 << 20
+    assert wl.B * wl.H * wl.T * wl.dv * wl.dk * 4 == 32 << 20
     init = synth.initial_layer(wl, 0)
     ref = lib.NonReplayLayer(d, init["state"], init["state_idx"])                   # torch-allocated snapshots
     state = init["state"].cuda().contiguous()
@@ -67,6 +67,6 @@ def test_static_step_matches_the_allocating_calls_twice_in_a_row():
 def test_static_step_rejects_steps_beyond_its_area():
     import speculative_decode_recurrent_gb300 as lib
     so = lib.load()
-    big = dataclasses.replace(synth.WORKLOADS["b8"], name="b8_static_big", B=5, H=16)  # 40 MiB of snapshots
+    big = dataclasses.replace(synth.WORKLOADS["b8"], name="b8_static_big", B=3, H=16)  # 48 MiB of snapshots
     fake = ctypes.c_void_p(0x10000)                     # never dereferenced: the size check comes first
     assert so.gdn_nonreplay_step_static(ctypes.byref(_dims(lib, big)), *([fake] * 10), None) == -2
