@@ -389,28 +389,32 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
         const int lim = !live ? 0 : is_q ? min(p + 1, C) : row;
         float *dst = is_q ? sMm + (writes ? t2 : 0) * CMAX : sAm + row * CMAX;
         const int cbeg = (!kSplitKK || warp < 2) ? 0 : ca, cend = (!kSplitKK || warp >= 2) ? CMAX : ca;
+        const int r0 = (kSplitKK ? (warp & 1) : warp) * 32;         // the warp's first row
 #pragma unroll
         for (int cb = 0; cb < CMAX / 16; ++cb) {
             const int c0 = cb * 16;
             if (c0 < cbeg || c0 >= cend) continue;                // warp-uniform
-            float kq[16];
-            if (c0 < CP) {
-                tmem_ld16(lane_base + c0, kq);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) kq[j] = 0.f;
-            }
+            // zeros for the whole warp (no exponentials; the stage is issue-bound): no
+            // column below C, or only key rows, none of them past the block's first column
+            const bool zero = c0 >= C || (r0 + 32 <= C && c0 >= r0 + 31);
             float mrow[16];
+            if (zero) {
 #pragma unroll
-            for (int j4 = 0; j4 < 4; ++j4) {
-                const float4 x = *reinterpret_cast<const float4 *>(sGh + c0 + 4 * j4);
-                const float4 y = *reinterpret_cast<const float4 *>(sGl + c0 + 4 * j4);
-                const float gs[4] = {x.x, x.y, x.z, x.w}, ls[4] = {y.x, y.y, y.z, y.w};
+                for (int j = 0; j < 16; ++j) mrow[j] = 0.f;
+            } else {
+                float kq[16];
+                tmem_ld16(lane_base + c0, kq);                    // c0 < C <= CP
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int s = c0 + 4 * j4 + j;
-                    const float e = __expf((gh - gs[j]) + (gl - ls[j]));
-                    mrow[4 * j4 + j] = s < lim ? scl * e * kq[4 * j4 + j] : 0.f;
+                for (int j4 = 0; j4 < 4; ++j4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(sGh + c0 + 4 * j4);
+                    const float4 y = *reinterpret_cast<const float4 *>(sGl + c0 + 4 * j4);
+                    const float gs[4] = {x.x, x.y, x.z, x.w}, ls[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int s = c0 + 4 * j4 + j;
+                        const float e = __expf((gh - gs[j]) + (gl - ls[j]));
+                        mrow[4 * j4 + j] = s < lim ? scl * e * kq[4 * j4 + j] : 0.f;
+                    }
                 }
             }
             if (writes) {
