@@ -390,8 +390,8 @@ verify_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs 
         float *dst = is_q ? sMm + (writes ? t2 : 0) * CMAX : sAm + row * CMAX;
         const int cbeg = (!kSplitKK || warp < 2) ? 0 : ca, cend = (!kSplitKK || warp >= 2) ? CMAX : ca;
         const int r0 = (kSplitKK ? (warp & 1) : warp) * 32;         // the warp's first row
-#pragma unroll
-        for (int cb = 0; cb < CMAX / 16; ++cb) {
+#pragma unroll 1
+        for (int cb = 0; cb < CMAX / 16; ++cb) {                  // rolled: instruction fetch stalls lead
             const int c0 = cb * 16;
             if (c0 < cbeg || c0 >= cend) continue;                // warp-uniform
             // zeros for the whole warp (no exponentials; the stage is issue-bound): no
