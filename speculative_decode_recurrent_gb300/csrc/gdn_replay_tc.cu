@@ -989,7 +989,7 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
                 const int t = P::SPLIT ? (tid & 63) : tid;
                 const float gh = t < L ? sGh[t] : 0.f, gl = t < L ? sGl[t] : 0.f, bt = t < L ? sBeta[t] : 0.f;
                 const int cbeg = (!P::SPLIT || warp < 2) ? 0 : ca, cend = (!P::SPLIT || warp >= 2) ? CMAX : ca;
-#pragma unroll
+#pragma unroll 1
                 for (int cb = 0; cb < CMAX / 16; ++cb) {
                     const int c0 = cb * 16;
                     if (c0 < cbeg || c0 >= cend) continue;        // warp-uniform
@@ -1108,7 +1108,7 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
             // ---- R'[d_v = tid][s] = -gamma_s (S0 k_s) as two bf16 terms (the value part of r
             //      enters the contraction directly: r_s = beta_s v_s + beta_s R'_s, and beta
             //      is folded into F)
-#pragma unroll
+#pragma unroll 1
             for (int cb = 0; cb < CMAX / 16; ++cb) {
                 if (cb < nb) {
                     float pk[16];
@@ -1181,7 +1181,7 @@ fold_eq_kernel(const __grid_constant__ CUtensorMap tm_state, const ReplayArgs a)
             }
             tc_fence_after();
             // ---- E^T row d_k = tid as two bf16 terms, K-major [128][64] tiles
-#pragma unroll
+#pragma unroll 1
             for (int cb = 0; cb < CMAX / 16; ++cb) {
                 if (cb < nb) {
                     float ev[16];
