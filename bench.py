@@ -45,9 +45,9 @@ FALLBACK_HBM_GBS = 6800.0
 # dram read+write bytes per verify launch from the ncu capture summarised in
 # profiles/; valid only for the kernel source whose hash is recorded with it.
 NCU_TRAFFIC = {         # {(step mode, source_sha1): dram read + write bytes per launch}
-    ("overlap", "97a1aa225dc8ca90df42bd3a89f5944a8855e22e"): 43.33e6,      # verify_eq_kernel<48>, profiles/verify_dram_decode24.md
-    ("three_call", "97a1aa225dc8ca90df42bd3a89f5944a8855e22e"): 43.32e6,   # verify_eq_kernel<48>, same capture
-    ("fused", "97a1aa225dc8ca90df42bd3a89f5944a8855e22e"): 48.93e6,        # fold launch 16.52 MB + verify launch 32.41 MB
+    ("overlap", "385240111fdd5c5cf53858ae6a847d7b97404e00"): 43.32e6,      # verify_eq_kernel<48>, profiles/verify_dram_decode24.md
+    ("three_call", "385240111fdd5c5cf53858ae6a847d7b97404e00"): 43.33e6,   # verify_eq_kernel<48>, same capture
+    ("fused", "385240111fdd5c5cf53858ae6a847d7b97404e00"): 48.91e6,        # fold launch 16.52 MB + verify launch 32.41 MB
 }
 
 
