@@ -51,20 +51,22 @@ def test_decode24_layers_first_and_last(layer):
 
 
 def test_large_batch_sampled_rows():
-    """B=128, H=32, T=8 on the GPU at full size; the oracle recomputes a
-    sample of the sequences (they are independent) for every checked tensor."""
+    """B=128, H=32, T=8 on the GPU at full size for 24 steps (every sampled sequence
+    folds at least twice); the oracle recomputes 12 of the sequences (they are
+    independent) for every checked tensor."""
     wl = WL["large"]
     import speculative_decode_recurrent_gb300 as lib
     init = synth.initial_layer(wl, 0)
     from harness import gpu_dims, oracle_dims
     gd = gpu_dims(wl)
     gpu = lib.ReplayLayer(gd, init)
-    sample = np.array([0, 1, 37, 64, 100, 127])
+    sample = np.array([0, 1, 9, 23, 37, 50, 64, 77, 90, 100, 111, 127])
     sub = dict(init)
     sub["state_idx"] = init["state_idx"][sample]
     od = oracle_dims(wl, B=len(sample), n_slot=gd.n_slot)
     orc = oracle.Layer(od, sub)
-    for s in range(3):
+    folds = np.zeros(len(sample), np.int64)
+    for s in range(24):                                   # ~3 folds per sequence (T=8, threshold 32)
         blk = synth.draft_block(wl, 0, s)
         dev = {n: blk[n].cuda() for n in ("q", "k", "v", "g", "beta")}
         out = torch.empty(wl.B, wl.T, wl.H, wl.dv, device="cuda")
@@ -73,14 +75,17 @@ def test_large_batch_sampled_rows():
         o_ref = orc.verify(sblk)
         gpu.accept(blk["accepted"].cuda())
         orc.accept(blk["accepted"][sample].numpy())
+        slots = init["state_idx"][sample].long().numpy()
+        before = orc.buf_len[slots].copy()
         gpu.flush()
         orc.flush()
+        folds += orc.buf_len[slots] < before
         torch.cuda.synchronize()
         assert_close(f"out step{s}", to_np(out)[sample], o_ref)
-        slots = init["state_idx"][sample].long().numpy()
         assert_close(f"state step{s}", to_np(gpu.t["state"])[slots], orc.state[slots])
         np.testing.assert_array_equal(gpu.t["buf_len"].cpu().numpy()[slots], orc.buf_len[slots])
         assert int(gpu.status.item()) == 0
+    assert folds.min() >= 2, folds
 
 
 # ------------------------------------------------------------ exact invariants
