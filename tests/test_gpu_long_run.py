@@ -5,6 +5,9 @@ T=16, flush threshold 32), against the fp64 CPU oracle at every step:
   flush) and in the fused step (verify_fold -> accept_fold), so each sequence goes
   through 15-20 flushes and the error of the tf32 checkpoint contractions has that
   many chances to compound;
+* the threshold-64 mix (buffers up to 79 tokens) and a threshold-48 B=8 layer (buffers
+  up to 63 tokens) for 48 steps each, so the 80- and 64-token variants of both kernels
+  fold every sequence several times;
 * the overlapped schedule the benchmark times (verifies on the capturing stream,
   each layer's accept + flush on one of two side streams, captured in a CUDA graph)
   on three layers for 20 steps, every layer compared with its own oracle;
@@ -108,6 +111,34 @@ def test_edge_48_steps_long_buffers(form):
         _record(name, s)
     assert folds.min() >= 3, folds
     assert longest + wl.T > 64, longest          # verifies over more than 64 tokens happened
+    _LOG[name + "_folds_per_sequence"] = [int(folds.min()), int(folds.max())]
+
+
+@pytest.mark.parametrize("form", ["three_call", "fused"])
+def test_cap63_48_steps(form):
+    """B=8 with threshold 48 (buffers of up to 63 tokens: the 64-token variants of both
+    tensor-core kernels, four 16-token blocks in the inverse) for 48 steps."""
+    import dataclasses
+    wl = dataclasses.replace(WL["b8"], name="b8_cap63_long", threshold=48)
+    pr = Pair(wl)
+    name = f"cap63_{form}"
+    DRIFT.clear()
+    idx = pr.gpu.t["state_idx"].long()
+    folds = np.zeros(wl.B, np.int64)
+    longest = 0
+    for s in range(48):
+        before = pr.gpu.t["buf_len"][idx].cpu().numpy()
+        longest = max(longest, int(before.max()))
+        if form == "three_call":
+            pr.step(s)
+            after = pr.gpu.t["buf_len"][idx].cpu().numpy()
+            folds += after < before + pr.block(s)["accepted"].numpy()
+        else:
+            pr.fused_step(s)
+            folds += before >= wl.threshold
+        _record(name, s)
+    assert folds.min() >= 3, folds
+    assert longest + wl.T > 48, longest          # verifies over more than 48 tokens happened
     _LOG[name + "_folds_per_sequence"] = [int(folds.min()), int(folds.max())]
 
 
