@@ -3,7 +3,7 @@ T=16, flush threshold 32), against the fp64 CPU oracle at every step:
 
 * layers 0 and 23 over all 64 steps, in the three-call step (verify -> accept ->
   flush) and in the fused step (verify_fold -> accept_fold), so each sequence goes
-  through 15-20 flushes and the error of the tf32 checkpoint contractions has that
+  through 12-18 flushes and the error of the tf32 checkpoint contractions has that
   many chances to compound;
 * the threshold-64 mix (buffers up to 79 tokens) and a threshold-48 B=8 layer (buffers
   up to 63 tokens) for 48 steps each, so the 80- and 64-token variants of both kernels
