@@ -225,12 +225,13 @@ class ReplayLayer:
 
     ``init`` is a dict of CPU tensors with the layouts of ``include/gdnreplay.h``
     (state, state_idx, buf_k, buf_v, buf_g, buf_beta, buf_len); they are copied
-    to ``device`` once.  The three methods enqueue the library calls.
+    to ``device`` once.  A state_idx of None is the identity map (sequence b owns
+    slot b).  The methods enqueue the library calls.
     """
 
     def __init__(self, dims: Dims, init: dict, device="cuda"):
         self.d = dims
-        self.t = {n: init[n].to(device).contiguous() for n in
+        self.t = {n: None if init[n] is None else init[n].to(device).contiguous() for n in
                   ("state", "state_idx", "buf_k", "buf_v", "buf_g", "buf_beta", "buf_len")}
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
 
@@ -355,11 +356,13 @@ def gdn_conv_accept(d: ConvDims, ring_pos, state_idx, accepted, status, stream=N
 
 class ConvLayer:
     """Device-resident convolution ring, write positions, weight and bias of one
-    layer (``init``: CPU tensors ring, pos, state_idx, weight, bias)."""
+    layer (``init``: CPU tensors ring, pos, state_idx, weight, bias; a state_idx of
+    None is the identity map)."""
 
     def __init__(self, dims: ConvDims, init: dict, device="cuda"):
         self.d = dims
-        self.t = {n: init[n].to(device).contiguous() for n in ("ring", "pos", "state_idx", "weight")}
+        self.t = {n: None if init[n] is None else init[n].to(device).contiguous()
+                  for n in ("ring", "pos", "state_idx", "weight")}
         self.t["bias"] = None if init.get("bias") is None else init["bias"].to(device).contiguous()
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
 
