@@ -252,6 +252,18 @@ def _step_layer(layer, wl, s):
     return out
 
 
+@pytest.mark.parametrize("name", ["b8", "edge"])
+def test_forced_flush_folds_short_buffers(name):
+    """flush(force=True) folds every non-empty buffer whatever its length: the first
+    step folds 0 .. 47 tokens (initial lengths 0..31 plus the accepted counts), every
+    later one 1..16 (edge: also 0, nothing to fold), so the tensor-core fold runs on
+    short and partial token blocks; checkpoint, buffer, lengths and outputs against the
+    oracle at every step."""
+    pr = Pair(WL[name])
+    for s in range(6):
+        pr.step(s, force=True)
+
+
 def test_bad_slot_reported_not_dereferenced():
     pr = Pair(WL["b8"])
     pr.gpu.t["state_idx"][3] = pr.gd.n_slot + 100
