@@ -2,6 +2,8 @@
 same seeded inputs.  Outputs and flushed state within
 max|d| <= 2e-3 max|ref| + 1e-5 per tensor per (layer, step); lengths, status
 words and buffer contents bit-exact."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -262,6 +264,21 @@ def test_forced_flush_folds_short_buffers(name):
     pr = Pair(WL[name])
     for s in range(6):
         pr.step(s, force=True)
+
+
+@pytest.mark.parametrize("T", [1, 3, 11])
+def test_short_drafts_on_the_tensor_cores(T):
+    """Draft blocks of 1, 3 and 11 tokens (the tensor-core kernels take T <= 16; one
+    token is the degenerate verify, W a single row), three-call then fused, 8 steps each."""
+    import speculative_decode_recurrent_gb300 as lib
+    wl = dataclasses.replace(WL["b8"], name=f"b8_T{T}", B=4, H=4, T=T)
+    pr = Pair(wl)
+    assert lib.gdn_replay_kernel_family(pr.gd) == lib.FAMILY_TCGEN05
+    for s in range(8):
+        pr.step(s)
+    pr = Pair(wl)
+    for s in range(8):
+        pr.fused_step(s)
 
 
 def test_bad_slot_reported_not_dereferenced():
