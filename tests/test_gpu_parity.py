@@ -281,6 +281,23 @@ def test_short_drafts_on_the_tensor_cores(T):
         pr.fused_step(s)
 
 
+def test_one_sequence_odd_heads_on_the_tensor_cores():
+    """B = 1, H = 3: in the fused steps where the only sequence folds, every CTA of the
+    verify launch beside the fold launch has nothing to do and leaves at once (its CTA
+    (0, 0) still waits for the fold launch); 12 steps three-call, 12 fused."""
+    wl = dataclasses.replace(WL["b8"], name="b1_h3", B=1, H=3)
+    pr = Pair(wl)
+    for s in range(12):
+        pr.step(s)
+    pr = Pair(wl)
+    folded = 0
+    for s in range(12):
+        before = int(pr.gpu.t["buf_len"][pr.gpu.t["state_idx"][0]].item())
+        pr.fused_step(s)
+        folded += before >= wl.threshold
+    assert folded >= 2
+
+
 def test_bad_slot_reported_not_dereferenced():
     pr = Pair(WL["b8"])
     pr.gpu.t["state_idx"][3] = pr.gd.n_slot + 100
