@@ -298,6 +298,32 @@ def test_one_sequence_odd_heads_on_the_tensor_cores():
     assert folded >= 2
 
 
+def test_length_boundaries():
+    """Buffer lengths at the edges (capacity 47, threshold 32): a fused step from 31 (no
+    fold; its verify takes 47 tokens, the capacity), 32 (exactly the threshold: folds),
+    47 (a full buffer: folds) and 0; then one where every sequence folds, so the
+    verify launch beside the fold launch has nothing to do; a three-call step from 31, 0,
+    1 and 15."""
+    wl = dataclasses.replace(WL["b8"], name="b8_edges", B=4, H=4)
+
+    def set_lens(pr, vals):
+        idx = pr.gpu.t["state_idx"].long().cpu()
+        for b, v in enumerate(vals):
+            pr.gpu.t["buf_len"][idx[b]] = v
+            pr.orc.buf_len[int(idx[b])] = v
+
+    pr = Pair(wl)
+    set_lens(pr, [31, 32, 47, 0])
+    pr.fused_step(0)
+    set_lens(pr, [40, 33, 47, 32])
+    pr.fused_step(1)
+    pr.fused_step(2)
+    pr = Pair(wl)
+    set_lens(pr, [31, 0, 1, 15])
+    pr.step(3)
+    pr.step(4)
+
+
 def test_bad_slot_reported_not_dereferenced():
     pr = Pair(WL["b8"])
     pr.gpu.t["state_idx"][3] = pr.gd.n_slot + 100
