@@ -298,13 +298,15 @@ def test_one_sequence_odd_heads_on_the_tensor_cores():
     assert folded >= 2
 
 
-def test_length_boundaries():
-    """Buffer lengths at the edges (capacity 47, threshold 32): a fused step from 31 (no
-    fold; its verify takes 47 tokens, the capacity), 32 (exactly the threshold: folds),
-    47 (a full buffer: folds) and 0; then one where every sequence folds, so the
-    verify launch beside the fold launch has nothing to do; a three-call step from 31, 0,
-    1 and 15."""
-    wl = dataclasses.replace(WL["b8"], name="b8_edges", B=4, H=4)
+@pytest.mark.parametrize("name,threshold", [("b8", 32), ("b8", 48), ("edge", 64)])
+def test_length_boundaries(name, threshold):
+    """Buffer lengths at the edges of each kernel variant (capacity = threshold + 15:
+    47, 63, 79 tokens): a fused step from threshold - 1 (no fold; its verify takes
+    the whole capacity), the threshold (folds), the capacity (a full buffer: folds) and
+    0; then one where every sequence folds, so the verify launch beside the fold launch
+    has nothing to do; a three-call step from threshold - 1, 0, 1 and 15."""
+    wl = dataclasses.replace(WL[name], name=f"{name}_edges{threshold}", B=4, H=4, threshold=threshold)
+    thr, cap = wl.threshold, wl.cap
 
     def set_lens(pr, vals):
         idx = pr.gpu.t["state_idx"].long().cpu()
@@ -312,14 +314,15 @@ def test_length_boundaries():
             pr.gpu.t["buf_len"][idx[b]] = v
             pr.orc.buf_len[int(idx[b])] = v
 
+    assert cap == thr + 15
     pr = Pair(wl)
-    set_lens(pr, [31, 32, 47, 0])
+    set_lens(pr, [thr - 1, thr, cap, 0])
     pr.fused_step(0)
-    set_lens(pr, [40, 33, 47, 32])
+    set_lens(pr, [cap - 7, thr + 1, cap, thr])
     pr.fused_step(1)
     pr.fused_step(2)
     pr = Pair(wl)
-    set_lens(pr, [31, 0, 1, 15])
+    set_lens(pr, [thr - 1, 0, 1, 15])
     pr.step(3)
     pr.step(4)
 
