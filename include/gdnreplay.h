@@ -105,7 +105,12 @@ typedef struct {
     int32_t dk;         /* key/query head dim: 64 or 128 */
     int32_t dv;         /* value head dim (state rows): 64 or 128 */
     int32_t T;          /* draft block length, 1..64 */
-    int32_t cap;        /* buffer slots per (slot, head), T <= cap <= 256 */
+    int32_t cap;        /* buffer slots per (slot, head), T <= cap <= 256; the per-token
+                           kernels hold the buffer and the draft in shared memory, so
+                           (cap (dk + dv + 2) + T dk) 4 bytes must fit in 227 KB (else
+                           GDN_ERR_DIMS), with cap + T in place of cap for
+                           gdn_replay_verify_fold: at dk = dv = 128, T = 16, cap <= 217,
+                           and <= 201 for the fused step */
     int32_t threshold;  /* flush when buf_len >= threshold, 1..cap */
     int32_t n_slot;     /* state / buffer slots, >= B */
     int32_t in_dtype;   /* GDN_DTYPE_BF16 or GDN_DTYPE_F32 */

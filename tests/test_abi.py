@@ -91,6 +91,20 @@ def test_bad_dims_rejected_before_launch(kw, code):
     assert so.gdn_replay_flush(ctypes.byref(d), *([FAKE] * 7), 0, FAKE, None) == code
 
 
+def test_pertoken_shared_memory_capacity():
+    """The per-token kernels hold the buffer and the draft in shared memory: at
+    dk = dv = 128 and T = 16 they take buffers of up to 217 tokens; at d = 64 the whole
+    range up to 256 (even with T = 64)."""
+    so = lib.load()
+    ok = good_dims(T=16, cap=217, threshold=200)
+    assert so.gdn_replay_kernel_family(ctypes.byref(ok)) == lib.FAMILY_PERTOKEN
+    big = good_dims(T=16, cap=218, threshold=200)
+    assert so.gdn_replay_kernel_family(ctypes.byref(big)) == -2
+    assert so.gdn_replay_verify(ctypes.byref(big), *([FAKE] * 14), None) == -2
+    d64 = good_dims(dk=64, dv=64, T=64, cap=256, threshold=200)
+    assert so.gdn_replay_kernel_family(ctypes.byref(d64)) == lib.FAMILY_PERTOKEN
+
+
 def test_fold_entry_points_validate():
     so = lib.load()
     d = good_dims(threshold=6)                 # threshold - 1 + T = 9 > cap = 8

@@ -298,10 +298,11 @@ def test_one_sequence_odd_heads_on_the_tensor_cores():
     assert folded >= 2
 
 
-@pytest.mark.parametrize("name,threshold", [("b8", 32), ("b8", 48), ("edge", 64)])
+@pytest.mark.parametrize("name,threshold", [("b8", 32), ("b8", 48), ("edge", 64), ("b8", 186)])
 def test_length_boundaries(name, threshold):
     """Buffer lengths at the edges of each kernel variant (capacity = threshold + 15:
-    47, 63, 79 tokens): a fused step from threshold - 1 (no fold; its verify takes
+    47, 63, 79 tokens on the tensor cores; 201, the largest the per-token kernels take
+    in the fused step at d = 128): a fused step from threshold - 1 (no fold; its verify takes
     the whole capacity), the threshold (folds), the capacity (a full buffer: folds) and
     0; then one where every sequence folds, so the verify launch beside the fold launch
     has nothing to do; a three-call step from threshold - 1, 0, 1 and 15."""
