@@ -328,6 +328,31 @@ def test_length_boundaries(name, threshold):
     pr.step(4)
 
 
+def test_pertoken_largest_shape():
+    """The per-token kernels at their largest shape: d = 64, T = 64, capacity 256
+    (threshold 193), fp32 inputs; a fused step from lengths 192 (its verify takes all
+    256 slots) and 256 (a full buffer folds), then three-call steps with forced flushes
+    from 192 and 0."""
+    wl = dataclasses.replace(WL["tiny"], name="tiny_max", B=2, H=2, T=64, threshold=193,
+                             forced_flush=False)
+    assert wl.cap == 256
+
+    def set_lens(pr, vals):
+        idx = pr.gpu.t["state_idx"].long().cpu()
+        for b, v in enumerate(vals):
+            pr.gpu.t["buf_len"][idx[b]] = v
+            pr.orc.buf_len[int(idx[b])] = v
+
+    pr = Pair(wl)
+    set_lens(pr, [192, 256])
+    pr.fused_step(0)
+    pr.fused_step(1)
+    pr = Pair(wl)
+    set_lens(pr, [192, 0])
+    pr.step(2, force=True)
+    pr.step(3, force=True)
+
+
 def test_bad_slot_reported_not_dereferenced():
     pr = Pair(WL["b8"])
     pr.gpu.t["state_idx"][3] = pr.gd.n_slot + 100
