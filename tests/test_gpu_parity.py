@@ -52,10 +52,11 @@ def test_decode24_layers_first_and_last(layer):
         pr.step(s)
 
 
-def test_large_batch_sampled_rows():
+@pytest.mark.parametrize("form", ["three_call", "fused"])
+def test_large_batch_sampled_rows(form):
     """B=128, H=32, T=8 on the GPU at full size for 24 steps (every sampled sequence
-    folds at least twice); the oracle recomputes 12 of the sequences (they are
-    independent) for every checked tensor."""
+    folds at least twice), three-call or fused; the oracle recomputes 12 of the
+    sequences (they are independent) for every checked tensor."""
     wl = WL["large"]
     import speculative_decode_recurrent_gb300 as lib
     init = synth.initial_layer(wl, 0)
@@ -72,16 +73,25 @@ def test_large_batch_sampled_rows():
         blk = synth.draft_block(wl, 0, s)
         dev = {n: blk[n].cuda() for n in ("q", "k", "v", "g", "beta")}
         out = torch.empty(wl.B, wl.T, wl.H, wl.dv, device="cuda")
-        gpu.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], out)
         sblk = {n: blk[n][sample] for n in ("q", "k", "v", "g", "beta")}
-        o_ref = orc.verify(sblk)
-        gpu.accept(blk["accepted"].cuda())
-        orc.accept(blk["accepted"][sample].numpy())
         slots = init["state_idx"][sample].long().numpy()
-        before = orc.buf_len[slots].copy()
-        gpu.flush()
-        orc.flush()
-        folds += orc.buf_len[slots] < before
+        if form == "three_call":
+            gpu.verify(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], out)
+            o_ref = orc.verify(sblk)
+            gpu.accept(blk["accepted"].cuda())
+            orc.accept(blk["accepted"][sample].numpy())
+            before = orc.buf_len[slots].copy()
+            gpu.flush()
+            orc.flush()
+            folds += orc.buf_len[slots] < before
+        else:
+            gpu.verify_fold(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], out)
+            gpu.accept_fold(blk["accepted"].cuda())
+            before = orc.buf_len[slots].copy()
+            orc.flush()
+            folds += orc.buf_len[slots] < before
+            o_ref = orc.verify(sblk)
+            orc.accept(blk["accepted"][sample].numpy())
         torch.cuda.synchronize()
         assert_close(f"out step{s}", to_np(out)[sample], o_ref)
         assert_close(f"state step{s}", to_np(gpu.t["state"])[slots], orc.state[slots])
