@@ -75,12 +75,13 @@ int gdn_nonreplay_accept(const gdn_replay_dims *dims, float *state, const int32_
  * (updated in place), state_idx, q, k, v, g, beta, accepted, out, status.
  *
  * A step larger than GDN_NONREPLAY_STATIC_SNAP_BYTES of snapshots returns GDN_ERR_DIMS
- * before anything is launched.  The first call on each device looks up the area's
- * device address (set-up, once per device, with that device current); make that first
- * call before any stream capture.  Every call shares the one area and leaves its
- * snapshots there; nothing in it needs clearing (the verify writes every snapshot the
- * accept reads), but calls whose work overlaps on the GPU -- on different streams, or
- * from different threads -- race on it and must be serialised by the caller. */
+ * before anything is launched.  Every call looks up the area's device address in the
+ * current context (host-side, no synchronisation; the first lookup in a context loads
+ * the library's device code there, so make the first call before any stream capture).
+ * Every call shares the one area and leaves its snapshots there; nothing in it needs
+ * clearing (the verify writes every snapshot the accept reads), but calls whose work
+ * overlaps on the GPU -- on different streams, or from different threads -- race on it
+ * and must be serialised by the caller. */
 int gdn_nonreplay_step_static(const gdn_replay_dims *dims, float *state, const int32_t *state_idx,
                               const void *q, const void *k, const void *v, const float *g,
                               const float *beta, const int32_t *accepted, float *out, int32_t *status,

@@ -14,8 +14,6 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
-#include <mutex>
-
 #include "gdnnonreplay.h"
 #include "replay_common.h"
 
@@ -218,26 +216,18 @@ extern "C" int gdn_nonreplay_accept(const gdn_replay_dims *dims, float *state, c
 // The baseline step for callers that cannot allocate device memory: the snapshots
 // live in this fixed area (GDN_NONREPLAY_STATIC_SNAP_BYTES) instead of a caller
 // buffer.  Host code must not hand the array's name to a kernel -- on the host it is
-// only a stand-in for the symbol -- so its device address is looked up once per device.
+// only a stand-in for the symbol -- so its device address is looked up, on every call:
+// a context created after a device reset loads the library again, possibly elsewhere.
 static __device__ __align__(256) float g_static_snap[GDN_NONREPLAY_STATIC_SNAP_BYTES / sizeof(float)];
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-std::mutex g_static_snap_mu;
-float *g_static_snap_dev[kMaxDevices] = {};
-
-// Device address of g_static_snap on the current device (set-up on the first call).
+// Device address of g_static_snap in the current context (the first lookup in a
+// context loads the library's device code there).
 int static_snap_address(float **out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_LAUNCH;
-    std::lock_guard<std::mutex> lock(g_static_snap_mu);
-    if (!g_static_snap_dev[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_snap) != cudaSuccess || !p) return GDN_ERR_LAUNCH;
-        g_static_snap_dev[dev] = static_cast<float *>(p);
-    }
-    *out = g_static_snap_dev[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_snap) != cudaSuccess || !p) return GDN_ERR_LAUNCH;
+    *out = static_cast<float *>(p);
     return GDN_OK;
 }
 
