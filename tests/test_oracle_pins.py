@@ -400,3 +400,68 @@ def test_status_bits_and_skips():
     status[0] = 0
     oracle.accept(d, ln, idx, np.array([d.T, 0, 0], np.int32), status)   # len + p > cap
     assert status[0] == oracle.BAD_LEN
+
+
+# ------------------------------------------------- many steps against a plain model
+@pytest.mark.parametrize("seed", [11, 12, 13])
+def test_many_steps_against_a_matrix_form_model(seed):
+    """Twelve decode steps with random accepted counts (0..T), threshold flushes and a
+    forced flush every fifth step, against an independent model of the method written
+    with the textbook matrix form: per slot a checkpoint (rounded to fp32 when it is
+    rewritten) and the list of tokens committed since; a verify runs the matrix form
+    from the checkpoint over that list and the draft; an accept appends the first p
+    draft tokens; a flush of a list that reached the threshold (any non-empty one when
+    forced) replaces the checkpoint by the rounded state after it and empties the list.
+    The slot that no sequence owns must never change."""
+    d, idx, rng, (st, bk, bv, bg, bb, ln) = _setup(seed, T=3, cap=10, threshold=6)
+    model_S = {int(s): st[s].copy() for s in range(d.n_slot)}
+    model_list = {int(s): [(bk[s, :, t].copy(), bv[s, :, t].copy(), bg[s, :, t].copy(), bb[s, :, t].copy())
+                           for t in range(ln[s])] for s in range(d.n_slot)}
+    unused = [s for s in range(d.n_slot) if s not in idx]
+    st_unused = st[unused].copy()
+    status = np.zeros(1, np.int32)
+    folds = 0
+
+    def run(S, toks, q=None):
+        """S: [dv, dk] for one head; toks: (k, v, g, beta) per token for that head; the
+        output after each token whose query (q[i]) is given."""
+        outs = []
+        for i, (k, v, g, be) in enumerate(toks):
+            S = math.exp(g) * S @ (np.eye(d.dk) - be * np.outer(k, k)) + be * np.outer(v, k)
+            if q is not None and q[i] is not None:
+                outs.append(S @ (d.scale * q[i]))
+        return S, np.array(outs)
+
+    for step in range(12):
+        q, k, v, g, beta = _random_block(d, rng)
+        out = np.zeros((d.B, d.T, d.H, d.dv))
+        oracle.verify(d, st, idx, bk, bv, bg, bb, ln, q, k, v, g, beta, out, status)
+        for b in range(d.B):
+            s = int(idx[b])
+            for h in range(d.H):
+                toks = [(kk[h], vv[h], gg[h], be[h]) for kk, vv, gg, be in model_list[s]]
+                drafts = [(k[b, t, h], v[b, t, h], g[b, t, h], beta[b, t, h]) for t in range(d.T)]
+                _, o = run(model_S[s][h], toks + drafts, q=[None] * len(toks) + list(q[b, :, h]))
+                np.testing.assert_allclose(out[b, :, h], o, rtol=1e-9, atol=1e-12)
+        p = rng.integers(0, d.T + 1, d.B).astype(np.int32)
+        oracle.accept(d, ln, idx, p, status)
+        for b in range(d.B):
+            s = int(idx[b])
+            model_list[s] += [(k[b, t].copy(), v[b, t].copy(), g[b, t].copy(), beta[b, t].copy())
+                              for t in range(p[b])]
+        force = step % 5 == 4
+        oracle.flush(d, st, idx, bk, bv, bg, bb, ln, force, status)
+        for b in range(d.B):
+            s = int(idx[b])
+            n = len(model_list[s])
+            if n >= d.threshold or (force and n > 0):
+                model_S[s] = np.array([run(model_S[s][h], [(kk[h], vv[h], gg[h], be[h])
+                                                           for kk, vv, gg, be in model_list[s]])[0]
+                                       for h in range(d.H)]).astype(np.float32).astype(np.float64)
+                model_list[s] = []
+                folds += 1
+            assert ln[s] == len(model_list[s])
+            np.testing.assert_allclose(st[s], model_S[s], rtol=2.0 ** -22, atol=1e-30)
+        assert status[0] == 0
+        np.testing.assert_array_equal(st[unused], st_unused)
+    assert folds >= 6
